@@ -1,0 +1,181 @@
+/*
+ * attn.h - C ABI of the fused online-softmax attention library (libattn.so).
+ *
+ * The library computes O = softmax(s * Q K^T + bias + mask) V in one pass over
+ * the keys, keeping a running row max m, a running sum l and an output
+ * accumulator that is rescaled by exp(m_old - m_new) whenever the max grows
+ * (the repaired online softmax of Neptune论文浅读 (gentlecold.top) §3-§4).
+ * Two forms are exposed:
+ *   - prefill, the Rolling Update form (same page, §5): one kernel streams
+ *     K/V tiles past resident Q tiles;
+ *   - decode, the Split-K Update form (same page, §6): the key axis is split
+ *     into independent local reductions whose partial results are merged by
+ *     a separate combine call that repairs them with the global max.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device.
+ *   - bf16 tensors are row-major and contiguous, innermost dimension last:
+ *       Q [B, Hq, Lq, d]   K, V [B, Hkv, Lk, d]   O [B, Hq, Lq, d]
+ *     LSE is fp32 [B, Hq, Lq] and holds the natural-log log-sum-exp of each
+ *     row's scaled, biased, masked scores (m + ln l).
+ *   - GQA: query head h reads KV head h / (Hq / Hkv) (consecutive groups; the
+ *     stacked-heads layout of CMU 15-779 第 11 讲 §7.1). Hq must be a
+ *     multiple of Hkv.
+ *   - Ownership: the caller allocates and owns every buffer. The library
+ *     allocates no device or host memory, never frees, and never
+ *     synchronises except inside attn_device_status().
+ *   - Streams: every launch is asynchronous on the given stream
+ *     (cudaStream_t passed as void*, NULL = legacy default stream).
+ *   - Errors: arguments are validated before anything is launched; an
+ *     invalid call launches nothing and returns a non-zero attn_status.
+ *     A launch failure returns ATTN_ERR_CUDA. Kernels never trap: a device
+ *     wait that exceeds its time limit records ATTN_ERR_TIMEOUT in a device
+ *     status word and the kernel returns; attn_device_status() reads it.
+ *   - Supported head dims: d in {64, 128}. Pointers must be 16-byte aligned.
+ */
+#ifndef ATTN_H
+#define ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = 1,          /* a required pointer is NULL               */
+    ATTN_ERR_SHAPE = 2,         /* a size is <= 0, or Hq % Hkv != 0, ...    */
+    ATTN_ERR_UNSUPPORTED = 3,   /* head dim or implementation not built     */
+    ATTN_ERR_WORKSPACE = 4,     /* split count out of range                  */
+    ATTN_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed         */
+    ATTN_ERR_TIMEOUT = 6,       /* a device wait hit its time limit          */
+    ATTN_ERR_ALIGN = 7,         /* pointer not 16-byte aligned               */
+    ATTN_ERR_VALUE = 8          /* scale not finite, or similar              */
+} attn_status;
+
+/* Prefill implementations selectable through attn_prefill_ex. */
+enum {
+    ATTN_IMPL_AUTO = 0,         /* the fastest built kernel for the shape    */
+    ATTN_IMPL_TCGEN05 = 1,      /* warp-specialised tcgen05/TMEM/TMA kernel  */
+    ATTN_IMPL_MMA_SYNC = 2      /* register-tile mma.sync kernel             */
+};
+
+/*
+ * attn_prefill - fused attention forward, Rolling Update form.
+ *
+ * Defines: the attention chain QK^T -> score/mask/bias -> softmax -> .V of
+ * Neptune论文浅读 §2, fused along the key axis as in its §5 and in the
+ * three-level loop of the CANN FlashAttention blog (ai6s.net), section
+ * "ops-transformer在昇腾NPU上的工程处理": an outer loop over Q blocks, an
+ * inner loop over K/V blocks with the online softmax state updated per block.
+ *
+ *   Q      bf16 [B, Hq, Lq, d]      (device, read)
+ *   K, V   bf16 [B, Hkv, Lk, d]     (device, read)
+ *   O      bf16 [B, Hq, Lq, d]      (device, written; rounded to nearest even)
+ *   LSE    fp32 [B, Hq, Lq] or NULL (device, written when non-NULL)
+ *   causal non-zero: query row i sees keys j <= i + (Lk - Lq) (bottom-right
+ *          aligned); rows that see no key get O = 0, LSE = -inf.
+ *   scale  softmax scale s applied to Q K^T (must be finite).
+ *   alibi_slopes  NULL, or fp32 [Hq] on the device: adds
+ *          -slope[h] * |i + (Lk - Lq) - j| to the scaled score (not scaled).
+ *   stream cudaStream_t.
+ * Returns ATTN_OK or an attn_status error code.
+ */
+int attn_prefill(const void* Q, const void* K, const void* V,
+                 void* O, float* LSE,
+                 int B, int Hq, int Hkv, int Lq, int Lk, int d,
+                 int causal, float scale, const float* alibi_slopes,
+                 void* stream);
+
+/* As attn_prefill, with an explicit implementation (ATTN_IMPL_*).
+ * Returns ATTN_ERR_UNSUPPORTED when that implementation cannot run the shape. */
+int attn_prefill_ex(const void* Q, const void* K, const void* V,
+                    void* O, float* LSE,
+                    int B, int Hq, int Hkv, int Lq, int Lk, int d,
+                    int causal, float scale, const float* alibi_slopes,
+                    int impl, void* stream);
+
+/*
+ * Split-K decode (Neptune论文浅读 §6; the split-KV decode of CMU 15-779
+ * 第 11 讲 §7.1, which parallelises over batch x KV head x KV sequence and
+ * stacks the G = Hq / Hkv query heads of a group as rows so that each K/V row
+ * is read once per KV head).
+ *
+ * Split geometry: with S splits and padded length Lk_max, every split covers
+ * C = attn_decode_split_len(Lk_max, S) keys: split s covers keys
+ * [s*C, (s+1)*C) clipped to [0, kv_len[b]). Splits beyond a sequence's
+ * length are empty and produce LSE_part = -inf, O_part = 0.
+ */
+
+/* Resolves a requested split count: requested > 0 is returned unchanged
+ * (clipped to [1, Lk_max]); 0 picks a count for this shape and device.
+ * Returns the count, or a negative attn_status on invalid sizes. */
+int attn_decode_num_splits(int B, int Hkv, int Lk_max, int d, int requested);
+
+/* Keys per split: ceil(ceil(Lk_max / S) / 64) * 64, or a negative
+ * attn_status on invalid sizes. */
+int attn_decode_split_len(int Lk_max, int num_splits);
+
+/* Bytes of the two partial buffers together: fp32 O_part [B, Hq, S, d] plus
+ * fp32 LSE_part [B, Hq, S]. Returns 0 on invalid sizes. */
+size_t attn_decode_workspace_bytes(int B, int Hq, int num_splits, int d);
+
+/*
+ * attn_decode_splitk - local reductions of the Split-K form.
+ *
+ *   Q        bf16 [B, Hq, d]                 (device, read; one query token)
+ *   K, V     bf16 [B, Hkv, Lk_max, d]        (device, read; padded KV cache)
+ *   kv_lens  int32 [B] on the device, each in [0, Lk_max], or NULL (= Lk_max)
+ *   scale    softmax scale (finite)
+ *   num_splits  S as resolved by attn_decode_num_splits (0 = auto); the
+ *            count actually used is written to *out_splits when non-NULL.
+ *   O_part   fp32 [B, Hq, S, d]  (device, written): each split's normalised
+ *            output o_s / l_s
+ *   LSE_part fp32 [B, Hq, S]     (device, written): m_s + ln l_s, or -inf
+ * The caller sizes O_part / LSE_part for the resolved S.
+ */
+int attn_decode_splitk(const void* Q, const void* K, const void* V,
+                       const int* kv_lens,
+                       int B, int Hq, int Hkv, int Lk_max, int d, float scale,
+                       int num_splits, int* out_splits,
+                       float* O_part, float* LSE_part, void* stream);
+
+/*
+ * attn_combine - global reduction of the Split-K form (Neptune论文浅读 §6:
+ * every split's local sum and output is repaired with the global max, then
+ * summed). With M = max_s LSE_s and w_s = exp(LSE_s - M):
+ *   O = sum_s w_s O_s / sum_s w_s,   LSE = M + ln sum_s w_s.
+ * Splits with LSE_s = -inf weigh 0; if all are -inf, O = 0 and LSE = -inf.
+ *
+ *   O_part fp32 [B, Hq, S, d], LSE_part fp32 [B, Hq, S]  (device, read)
+ *   O      bf16 [B, Hq, d]                                (device, written)
+ *   LSE    fp32 [B, Hq] or NULL                           (device, written)
+ */
+int attn_combine(const float* O_part, const float* LSE_part,
+                 int B, int Hq, int S, int d,
+                 void* O, float* LSE, void* stream);
+
+/* Convenience: attn_decode_splitk followed by attn_combine on one stream,
+ * with caller-provided partial buffers sized for the resolved S. */
+int attn_decode(const void* Q, const void* K, const void* V, const int* kv_lens,
+                int B, int Hq, int Hkv, int Lk_max, int d, float scale,
+                int num_splits, float* O_part, float* LSE_part,
+                void* O, float* LSE, void* stream);
+
+/* Static text for a status code (never NULL). */
+const char* attn_status_string(int status);
+
+/* Synchronises `stream`, then returns and clears the device status word of
+ * the current device (ATTN_OK when no kernel recorded an error), or
+ * ATTN_ERR_CUDA when synchronisation itself failed. */
+int attn_device_status(void* stream);
+
+/* Library ABI version (major * 100 + minor). */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H */

@@ -1,0 +1,216 @@
+"""Python binding of libattn.so (fused online-softmax attention for GB300).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libattn.so. PyTorch supplies device memory and the current stream.
+If the library is not built, importing works but every call raises; there is
+no fallback path.
+
+Entry points mirror include/attn.h:
+    prefill(q, k, v, causal, scale, alibi_slopes, impl)  -> (O, LSE)
+    decode_splitk(q, k, v, kv_lens, scale, num_splits)   -> (O_part, LSE_part)
+    combine(O_part, LSE_part)                            -> (O, LSE)
+    decode(q, k, v, kv_lens, scale, num_splits)          -> (O, LSE)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn.so")
+
+ATTN_OK = 0
+IMPLS = {"auto": 0, "tcgen05": 1, "mma_sync": 2}
+
+_c_void_p = ctypes.c_void_p
+_c_int = ctypes.c_int
+_c_float = ctypes.c_float
+
+# name -> (restype, argtypes); the full exported surface of include/attn.h
+SIGNATURES = {
+    "attn_prefill": (_c_int, [_c_void_p] * 5 + [_c_int] * 7 + [_c_float, _c_void_p, _c_void_p]),
+    "attn_prefill_ex": (_c_int, [_c_void_p] * 5 + [_c_int] * 7 + [_c_float, _c_void_p, _c_int,
+                                                                   _c_void_p]),
+    "attn_decode_num_splits": (_c_int, [_c_int] * 5),
+    "attn_decode_split_len": (_c_int, [_c_int] * 2),
+    "attn_decode_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
+    "attn_decode_splitk": (_c_int, [_c_void_p] * 4 + [_c_int] * 5 + [_c_float, _c_int, _c_void_p,
+                                                                     _c_void_p, _c_void_p,
+                                                                     _c_void_p]),
+    "attn_combine": (_c_int, [_c_void_p] * 2 + [_c_int] * 4 + [_c_void_p] * 3),
+    "attn_decode": (_c_int, [_c_void_p] * 4 + [_c_int] * 5 + [_c_float, _c_int] + [_c_void_p] * 5),
+    "attn_status_string": (ctypes.c_char_p, [_c_int]),
+    "attn_device_status": (_c_int, [_c_void_p]),
+    "attn_version": (_c_int, []),
+}
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = lib().attn_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libattn.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m online_softmax_fusion_gb300.build` (no fallback path exists)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != ATTN_OK:
+        raise AttnError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _req(t, name, dtype, dims):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dims, got {t.dim()}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def prefill(q, k, v, causal=False, scale=None, alibi_slopes=None, impl="auto", out=None,
+            lse=None, with_lse=True):
+    """Fused attention forward. q [B,Hq,Lq,d], k/v [B,Hkv,Lk,d] bf16 CUDA.
+    Returns (O bf16 [B,Hq,Lq,d], LSE fp32 [B,Hq,Lq] or None)."""
+    _req(q, "q", torch.bfloat16, 4)
+    _req(k, "k", torch.bfloat16, 4)
+    _req(v, "v", torch.bfloat16, 4)
+    B, Hq, Lq, d = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k and v must be [B, Hkv, Lk, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if alibi_slopes is not None:
+        _req(alibi_slopes, "alibi_slopes", torch.float32, 1)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and with_lse:
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    st = lib().attn_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Lq,
+                               Lk, d, int(bool(causal)), float(scale), _ptr(alibi_slopes),
+                               IMPLS[impl], _stream())
+    _check(st, "attn_prefill")
+    return out, lse
+
+
+def resolve_splits(B, Hkv, Lk_max, d, requested=0) -> int:
+    s = lib().attn_decode_num_splits(B, Hkv, Lk_max, d, requested)
+    if s <= 0:
+        raise AttnError(-s, "attn_decode_num_splits")
+    return s
+
+
+def split_len(Lk_max, S) -> int:
+    c = lib().attn_decode_split_len(Lk_max, S)
+    if c <= 0:
+        raise AttnError(-c, "attn_decode_split_len")
+    return c
+
+
+def decode_splitk(q, k, v, kv_lens=None, scale=None, num_splits=0, o_part=None, lse_part=None):
+    """Split-K local reductions. q [B,Hq,d], k/v [B,Hkv,Lk_max,d] bf16 CUDA,
+    kv_lens int32 [B] CUDA or None. Returns (O_part fp32 [B,Hq,S,d],
+    LSE_part fp32 [B,Hq,S])."""
+    _req(q, "q", torch.bfloat16, 3)
+    _req(k, "k", torch.bfloat16, 4)
+    _req(v, "v", torch.bfloat16, 4)
+    B, Hq, d = q.shape
+    Hkv, Lk_max = k.shape[1], k.shape[2]
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k and v must be [B, Hkv, Lk_max, d] matching q")
+    if kv_lens is not None:
+        _req(kv_lens, "kv_lens", torch.int32, 1)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    S = resolve_splits(B, Hkv, Lk_max, d, num_splits)
+    if o_part is None:
+        o_part = torch.empty((B, Hq, S, d), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    out_s = ctypes.c_int(0)
+    st = lib().attn_decode_splitk(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_lens), B, Hq, Hkv, Lk_max, d,
+                                  float(scale), S, ctypes.byref(out_s), _ptr(o_part),
+                                  _ptr(lse_part), _stream())
+    _check(st, "attn_decode_splitk")
+    return o_part, lse_part
+
+
+def combine(o_part, lse_part, out=None, lse=None, with_lse=True):
+    """Log-sum-exp merge of split partials -> (O bf16 [B,Hq,d], LSE fp32 [B,Hq])."""
+    _req(o_part, "o_part", torch.float32, 4)
+    _req(lse_part, "lse_part", torch.float32, 3)
+    B, Hq, S, d = o_part.shape
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.bfloat16, device=o_part.device)
+    if lse is None and with_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=o_part.device)
+    st = lib().attn_combine(_ptr(o_part), _ptr(lse_part), B, Hq, S, d, _ptr(out), _ptr(lse),
+                            _stream())
+    _check(st, "attn_combine")
+    return out, lse
+
+
+def decode(q, k, v, kv_lens=None, scale=None, num_splits=0, o_part=None, lse_part=None,
+           out=None, lse=None):
+    """Split-K decode followed by the combine, on the current stream."""
+    _req(q, "q", torch.bfloat16, 3)
+    B, Hq, d = q.shape
+    Hkv, Lk_max = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    S = resolve_splits(B, Hkv, Lk_max, d, num_splits)
+    if o_part is None:
+        o_part = torch.empty((B, Hq, S, d), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _req(k, "k", torch.bfloat16, 4)
+    _req(v, "v", torch.bfloat16, 4)
+    if kv_lens is not None:
+        _req(kv_lens, "kv_lens", torch.int32, 1)
+    st = lib().attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_lens), B, Hq, Hkv, Lk_max, d,
+                           float(scale), S, _ptr(o_part), _ptr(lse_part), _ptr(out), _ptr(lse),
+                           _stream())
+    _check(st, "attn_decode")
+    return out, lse
+
+
+def device_status() -> int:
+    """Synchronises the current stream and returns/clears the device status word."""
+    return lib().attn_device_status(_stream())

@@ -1,0 +1,277 @@
+// C-ABI layer of libattn.so: argument validation, TMA descriptor encoding,
+// split-count policy, launch dispatch and the device status word.
+// The entry points are declared and documented in include/attn.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace attn {
+
+// First error recorded by any kernel of this library on this device.
+__device__ int g_status_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int* status_ptr() {
+    static int* ptrs[kMaxDevices] = {nullptr};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int*>(p);
+    }
+    return ptrs[dev];
+}
+
+int sm_count() {
+    static int counts[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
+    if (!counts[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 152;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// bf16 tensor [outer, L, d] (d innermost) as a 3-D tensor map with a
+// (64, box_rows, 1) box and the 128-byte swizzle; rows past L read as zero.
+int make_map(CUtensorMap* m, const void* base, int d, int L, long long outer, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return ATTN_ERR_CUDA;
+    cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(L), cuuint64_t(outer)};
+    cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(L) * cuuint64_t(d) * 2};
+    cuuint32_t box[3] = {64, cuuint32_t(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int Hq, int Hkv, int d, float scale) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0) return ATTN_ERR_SHAPE;
+    if (Hq % Hkv != 0) return ATTN_ERR_SHAPE;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return ATTN_ERR_VALUE;
+    if (B > 65535 || Hq > 65535) return ATTN_ERR_SHAPE;
+    return ATTN_OK;
+}
+
+int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
+
+}  // namespace
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+int attn_version(void) { return 100; }
+
+const char* attn_status_string(int status) {
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_NULL: return "a required pointer is NULL";
+        case ATTN_ERR_SHAPE: return "invalid sizes (non-positive, Hq not a multiple of Hkv, or too large)";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported head dim or implementation";
+        case ATTN_ERR_WORKSPACE: return "split count out of range";
+        case ATTN_ERR_CUDA: return "a CUDA call failed";
+        case ATTN_ERR_TIMEOUT: return "a device wait exceeded its time limit";
+        case ATTN_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case ATTN_ERR_VALUE: return "invalid value (scale not finite)";
+        default: return "unknown status";
+    }
+}
+
+int attn_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    }
+    return v;
+}
+
+int attn_prefill_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq,
+                    int Hkv, int Lq, int Lk, int d, int causal, float scale,
+                    const float* alibi_slopes, int impl, void* stream) {
+    if (!Q || !K || !V || !O) return ATTN_ERR_NULL;
+    int st = check_common(B, Hq, Hkv, d, scale);
+    if (st) return st;
+    if (Lq <= 0 || Lk <= 0) return ATTN_ERR_SHAPE;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return ATTN_ERR_ALIGN;
+    if ((LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) ||
+        (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)))
+        return ATTN_ERR_ALIGN;
+    if (impl < ATTN_IMPL_AUTO || impl > ATTN_IMPL_MMA_SYNC) return ATTN_ERR_UNSUPPORTED;
+
+    PrefillLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    L.p.O = static_cast<__nv_bfloat16*>(O);
+    L.p.LSE = LSE;
+    L.p.slopes = alibi_slopes;
+    L.p.B = B;
+    L.p.Hq = Hq;
+    L.p.Hkv = Hkv;
+    L.p.Lq = Lq;
+    L.p.Lk = Lk;
+    L.p.G = Hq / Hkv;
+    L.p.scale_log2 = scale * kLog2e;
+    L.p.causal = causal ? 1 : 0;
+    L.p.status = status_ptr();
+    if (!L.p.status) return ATTN_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    const bool want_tc = impl == ATTN_IMPL_TCGEN05 || impl == ATTN_IMPL_AUTO;
+    if (want_tc) {
+        if ((st = make_map(&L.tmQ, Q, d, Lq, (long long)B * Hq, kTcBM))) return st;
+        if ((st = make_map(&L.tmK, K, d, Lk, (long long)B * Hkv, kTcBN))) return st;
+        if ((st = make_map(&L.tmV, V, d, Lk, (long long)B * Hkv, kTcBN))) return st;
+        st = launch_prefill_tc(L, d, s);
+        if (st != ATTN_ERR_UNSUPPORTED || impl == ATTN_IMPL_TCGEN05) return st;
+    }
+    if ((st = make_map(&L.tmQ, Q, d, Lq, (long long)B * Hq, kMmaBM))) return st;
+    if ((st = make_map(&L.tmK, K, d, Lk, (long long)B * Hkv, kMmaBN))) return st;
+    if ((st = make_map(&L.tmV, V, d, Lk, (long long)B * Hkv, kMmaBN))) return st;
+    return launch_prefill_mma(L, d, s);
+}
+
+int attn_prefill(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq,
+                 int Hkv, int Lq, int Lk, int d, int causal, float scale, const float* alibi_slopes,
+                 void* stream) {
+    return attn_prefill_ex(Q, K, V, O, LSE, B, Hq, Hkv, Lq, Lk, d, causal, scale, alibi_slopes,
+                           ATTN_IMPL_AUTO, stream);
+}
+
+int attn_decode_split_len(int Lk_max, int num_splits) {
+    if (Lk_max <= 0) return -ATTN_ERR_SHAPE;
+    if (num_splits <= 0) return -ATTN_ERR_WORKSPACE;
+    const int per = ceil_div(Lk_max, num_splits);
+    return ceil_div(per, 64) * 64;
+}
+
+int attn_decode_num_splits(int B, int Hkv, int Lk_max, int d, int requested) {
+    if (B <= 0 || Hkv <= 0 || Lk_max <= 0) return -ATTN_ERR_SHAPE;
+    if (d != 64 && d != 128) return -ATTN_ERR_UNSUPPORTED;
+    if (requested < 0) return -ATTN_ERR_WORKSPACE;
+    if (requested > 0) return requested < Lk_max ? requested : Lk_max;
+    // Splits of about 2048 keys keep CTA work uniform across variable lengths;
+    // small batches split finer until there are ~8 CTAs per SM.
+    const int max_splits = ceil_div(Lk_max, 64);
+    int S = ceil_div(Lk_max, 2048);
+    const long long pairs = (long long)B * Hkv;
+    const long long target = 8LL * sm_count();
+    while (S < max_splits && pairs * S < target) S *= 2;
+    if (S > max_splits) S = max_splits;
+    return S;
+}
+
+size_t attn_decode_workspace_bytes(int B, int Hq, int num_splits, int d) {
+    if (B <= 0 || Hq <= 0 || num_splits <= 0 || d <= 0) return 0;
+    const size_t rows = size_t(B) * size_t(Hq) * size_t(num_splits);
+    return rows * size_t(d) * sizeof(float) + rows * sizeof(float);
+}
+
+int attn_decode_splitk(const void* Q, const void* K, const void* V, const int* kv_lens, int B,
+                       int Hq, int Hkv, int Lk_max, int d, float scale, int num_splits,
+                       int* out_splits, float* O_part, float* LSE_part, void* stream) {
+    if (!Q || !K || !V || !O_part || !LSE_part) return ATTN_ERR_NULL;
+    int st = check_common(B, Hq, Hkv, d, scale);
+    if (st) return st;
+    if (Lk_max <= 0) return ATTN_ERR_SHAPE;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O_part) ||
+        (reinterpret_cast<uintptr_t>(LSE_part) & 3u) ||
+        (kv_lens && (reinterpret_cast<uintptr_t>(kv_lens) & 3u)))
+        return ATTN_ERR_ALIGN;
+    const int S = attn_decode_num_splits(B, Hkv, Lk_max, d, num_splits);
+    if (S <= 0) return -S;
+    if (S > 12288) return ATTN_ERR_WORKSPACE;
+    const int G = Hq / Hkv;
+
+    DecodeLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    L.p.Q = static_cast<const __nv_bfloat16*>(Q);
+    L.p.kv_lens = kv_lens;
+    L.p.O_part = O_part;
+    L.p.LSE_part = LSE_part;
+    L.p.B = B;
+    L.p.Hq = Hq;
+    L.p.Hkv = Hkv;
+    L.p.Lk_max = Lk_max;
+    L.p.S = S;
+    L.p.C = attn_decode_split_len(Lk_max, S);
+    L.p.G = G;
+    L.p.nrg = ceil_div(G, 16);
+    L.p.rows = ceil_div(G, L.p.nrg);
+    L.p.scale_log2 = scale * kLog2e;
+    L.p.status = status_ptr();
+    if (!L.p.status) return ATTN_ERR_CUDA;
+    if ((long long)Hkv * L.p.nrg > 65535) return ATTN_ERR_SHAPE;
+    if ((st = make_map(&L.tmK, K, d, Lk_max, (long long)B * Hkv, 64))) return st;
+    if ((st = make_map(&L.tmV, V, d, Lk_max, (long long)B * Hkv, 64))) return st;
+    if (out_splits) *out_splits = S;
+    return launch_decode(L, d, static_cast<cudaStream_t>(stream));
+}
+
+int attn_combine(const float* O_part, const float* LSE_part, int B, int Hq, int S, int d, void* O,
+                 float* LSE, void* stream) {
+    if (!O_part || !LSE_part || !O) return ATTN_ERR_NULL;
+    if (B <= 0 || Hq <= 0) return ATTN_ERR_SHAPE;
+    if (S <= 0 || S > 12288) return ATTN_ERR_WORKSPACE;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(O_part) & 3u) || (reinterpret_cast<uintptr_t>(LSE_part) & 3u) ||
+        (reinterpret_cast<uintptr_t>(O) & 1u) || (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)))
+        return ATTN_ERR_ALIGN;
+    return launch_combine(O_part, LSE_part, B, Hq, S, d, O, LSE, static_cast<cudaStream_t>(stream));
+}
+
+int attn_decode(const void* Q, const void* K, const void* V, const int* kv_lens, int B, int Hq,
+                int Hkv, int Lk_max, int d, float scale, int num_splits, float* O_part,
+                float* LSE_part, void* O, float* LSE, void* stream) {
+    if (!O) return ATTN_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(O) & 1u) || (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)))
+        return ATTN_ERR_ALIGN;
+    int S = 0;
+    int st = attn_decode_splitk(Q, K, V, kv_lens, B, Hq, Hkv, Lk_max, d, scale, num_splits, &S,
+                                O_part, LSE_part, stream);
+    if (st) return st;
+    return attn_combine(O_part, LSE_part, B, Hq, S, d, O, LSE, stream);
+}
+
+}  // extern "C"

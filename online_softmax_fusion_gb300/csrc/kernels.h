@@ -1,0 +1,65 @@
+// Launch descriptors shared between the C-ABI layer (api.cu) and the kernel
+// translation units. Host-side only types plus the plain parameter structs
+// passed by value to the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace attn {
+
+struct DecodeParams {
+    const __nv_bfloat16* Q;   // [B, Hq, d]
+    const int* kv_lens;       // [B] or nullptr
+    float* O_part;            // [B, Hq, S, d]
+    float* LSE_part;          // [B, Hq, S]
+    int B, Hq, Hkv, Lk_max;
+    int S;                    // splits
+    int C;                    // keys per split (multiple of 64)
+    int G;                    // query heads per KV head
+    int rows;                 // query heads per CTA (<= 16)
+    int nrg;                  // CTAs per KV head along the heads (ceil(G / rows))
+    float scale_log2;         // softmax scale * log2(e)
+    int* status;              // device status word
+};
+
+struct DecodeLaunch {
+    CUtensorMap tmK;          // K as (d, Lk_max, B*Hkv), box (64, 64, 1), 128 B swizzle
+    CUtensorMap tmV;
+    DecodeParams p;
+};
+
+struct PrefillParams {
+    __nv_bfloat16* O;         // [B, Hq, Lq, d]
+    float* LSE;               // [B, Hq, Lq] or nullptr
+    const float* slopes;      // [Hq] or nullptr (ALiBi)
+    int B, Hq, Hkv, Lq, Lk, G;
+    float scale_log2;         // softmax scale * log2(e)
+    int causal;
+    int* status;
+};
+
+struct PrefillLaunch {
+    CUtensorMap tmQ;          // Q as (d, Lq, B*Hq), box (64, BM, 1), 128 B swizzle
+    CUtensorMap tmK;          // K as (d, Lk, B*Hkv), box (64, BN, 1)
+    CUtensorMap tmV;
+    PrefillParams p;
+};
+
+int launch_decode(const DecodeLaunch& L, int d, cudaStream_t stream);
+int launch_combine(const float* O_part, const float* LSE_part, int B, int Hq, int S, int d,
+                   void* O, float* LSE, cudaStream_t stream);
+
+// Register-tile (mma.sync) prefill: Q tile rows and K/V tile keys it expects
+// in the tensor-map boxes.
+constexpr int kMmaBM = 128;
+constexpr int kMmaBN = 64;
+int launch_prefill_mma(const PrefillLaunch& L, int d, cudaStream_t stream);
+
+// tcgen05 prefill: box rows for Q and K/V.
+constexpr int kTcBM = 128;
+constexpr int kTcBN = 128;
+int launch_prefill_tc(const PrefillLaunch& L, int d, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,131 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every function include/attn.h declares, and rejects invalid
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import online_softmax_fusion_gb300 as attn
+from online_softmax_fusion_gb300 import build as attn_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    attn_build.build()
+    return attn.lib()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_\s\*]*?\b(attn_[a-z0-9_]+)\s*\(",
+                             text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    declared = _declared_functions()
+    assert {"attn_prefill", "attn_decode_splitk", "attn_combine"} <= declared
+    for name in declared:
+        assert hasattr(L, name), name
+    # the binding declares the same surface
+    assert declared == set(attn.SIGNATURES)
+
+
+def test_status_strings(L):
+    for code in range(0, 9):
+        s = L.attn_status_string(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert L.attn_status_string(0) == b"ok"
+    assert L.attn_version() >= 100
+
+
+P = ctypes.c_void_p(4096)       # aligned dummy pointer; never dereferenced
+MIS = ctypes.c_void_p(4096 + 2)  # misaligned
+
+
+def _prefill(L, Q=P, K=P, V=P, O=P, LSE=None, B=1, Hq=4, Hkv=2, Lq=128, Lk=128, d=128,
+             causal=0, scale=0.1, slopes=None, impl=0):
+    return L.attn_prefill_ex(Q, K, V, O, LSE, B, Hq, Hkv, Lq, Lk, d, causal, scale, slopes, impl,
+                             None)
+
+
+def test_prefill_validation_before_launch(L):
+    assert _prefill(L, Q=None) == 1
+    assert _prefill(L, O=None) == 1
+    assert _prefill(L, B=0) == 2
+    assert _prefill(L, Lq=0) == 2
+    assert _prefill(L, Lk=-3) == 2
+    assert _prefill(L, Hq=3, Hkv=2) == 2
+    assert _prefill(L, d=96) == 3
+    assert _prefill(L, d=256) == 3
+    assert _prefill(L, scale=float("nan")) == 8
+    assert _prefill(L, scale=float("inf")) == 8
+    assert _prefill(L, K=MIS) == 7
+    assert _prefill(L, LSE=ctypes.c_void_p(4098)) == 7
+    assert _prefill(L, impl=7) == 3
+
+
+def test_decode_validation_before_launch(L):
+    def dec(Q=P, K=P, V=P, lens=None, B=2, Hq=8, Hkv=2, Lmax=1024, d=128, scale=0.1, S=0,
+            Op=P, Lp=P):
+        return L.attn_decode_splitk(Q, K, V, lens, B, Hq, Hkv, Lmax, d, scale, S, None, Op, Lp,
+                                    None)
+    assert dec(Q=None) == 1
+    assert dec(Op=None) == 1
+    assert dec(Hq=6, Hkv=4) == 2
+    assert dec(Lmax=0) == 2
+    assert dec(d=80) == 3
+    assert dec(S=-1) == 4
+    assert dec(scale=float("inf")) == 8
+    assert dec(V=MIS) == 7
+    assert L.attn_combine(None, P, 1, 1, 4, 128, P, None, None) == 1
+    assert L.attn_combine(P, P, 1, 1, 0, 128, P, None, None) == 4
+    assert L.attn_combine(P, P, 1, 1, 4, 32, P, None, None) == 3
+    assert L.attn_combine(P, P, 0, 1, 4, 128, P, None, None) == 2
+
+
+def test_valid_call_without_gpu_fails_cleanly(L):
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _prefill(L) == 5          # ATTN_ERR_CUDA, nothing launched, no crash
+
+
+def test_split_geometry(L):
+    # keys per split: ceil(ceil(Lk_max / S) / 64) * 64
+    for Lmax, S in [(131072, 64), (32768, 16), (1000, 3), (1, 1), (65, 2), (4096, 4096)]:
+        per = -(-Lmax // S)
+        assert L.attn_decode_split_len(Lmax, S) == -(-per // 64) * 64
+    assert L.attn_decode_split_len(0, 4) < 0
+    assert L.attn_decode_split_len(100, 0) < 0
+    assert L.attn_decode_num_splits(4, 8, 131072, 128, 64) == 64
+    assert L.attn_decode_num_splits(1, 1, 10, 128, 64) == 10
+    S = L.attn_decode_num_splits(64, 8, 32768, 128, 0)
+    assert S >= 16 and (S & (S - 1)) == 0
+    assert L.attn_decode_num_splits(0, 8, 32768, 128, 0) < 0
+    ws = L.attn_decode_workspace_bytes(4, 64, 64, 128)
+    assert ws == 4 * 64 * 64 * 128 * 4 + 4 * 64 * 64 * 4
+    assert L.attn_decode_workspace_bytes(0, 64, 64, 128) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    monkeypatch.setattr(attn, "_lib", None)
+    monkeypatch.setattr(attn, "LIB_PATH", "/nonexistent/libattn.so")
+    with pytest.raises(RuntimeError, match="no fallback"):
+        attn.lib()
+
+
+def test_binding_rejects_cpu_tensors(L):
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        attn.prefill(q, q, q)
