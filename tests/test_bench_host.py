@@ -1,0 +1,102 @@
+"""Host-side checks of the bench: work accounting pinned to the numbers the
+CMU 15-779 第 11 讲 page prints (§1.2, 练习 6; fixture tests/golden/
+traffic_model.json), brute-force causal pair counts, and the max/sum over
+ranks used for N > 1 (gloo, world size 2, CPU)."""
+import json
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "traffic_model.json")
+
+
+def test_single_head_traffic_model_matches_lecture():
+    g = json.load(open(GOLDEN))["single_head"]
+    N, d, e = g["N"], g["d"], g["elem_bytes"]
+    # score matrix written once and read once: "67 MB"
+    assert round(bench.score_round_trip_bytes(N, e) / 1e6) == g["score_round_trip_MB"]
+    # fused I/O of one head (Q, K, V read, O written): "4.2 MB"
+    assert round(bench.prefill_io_bytes(1, 1, 1, N, N, d, e) / 1e6, 1) == g["flash_io_MB"]
+    # two matmuls, non-causal: "8.6 GFLOP"
+    assert round(bench.prefill_flops(1, 1, N, N, d, causal=False) / 1e9, 1) == g["two_matmul_GFLOP"]
+
+
+def test_gqa_decode_traffic_matches_exercise():
+    g = json.load(open(GOLDEN))["gqa_decode"]
+    lens = [g["ctx"]] * g["batch"]
+    kv = bench.decode_kv_bytes(g["kv_heads"], lens, g["d"], g["elem_bytes"])
+    per_q = bench.decode_kv_bytes_per_query_head(g["kv_heads"] * g["group"], lens, g["d"],
+                                                 g["elem_bytes"])
+    assert round(kv / 1e6) == g["kv_MB"]
+    assert round(per_q / 1e6) == g["per_query_head_MB"]
+    assert round(per_q / (g["hbm_TBps"] * 1e12) * 1e6) == g["per_query_head_us"]
+    assert round(kv / (g["hbm_TBps"] * 1e12) * 1e6) == g["grouped_us"]
+
+
+@pytest.mark.parametrize("Lq,Lk", [(1, 1), (5, 5), (7, 12), (12, 7), (1, 100), (100, 1),
+                                   (4096, 4096), (300, 333)])
+def test_causal_pairs_brute_force(Lq, Lk):
+    n = sum(1 for i in range(Lq) for j in range(Lk) if j <= i + Lk - Lq)
+    assert bench.causal_pairs(Lq, Lk) == n
+
+
+def test_causal_mha_workload_flops():
+    # 4 * 128 * 4 * 32 * 4096 * 4097 / 2
+    assert bench.prefill_flops(4, 32, 4096, 4096, 128, True) == 4 * 128 * 4 * 32 * (4096 * 4097 // 2)
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    mx = bench.max_over_ranks(float(rank + 1) * 1.5, world)
+    sm = bench.sum_over_ranks(float(rank + 1), world)
+    q.put((rank, mx, sm))
+    dist.destroy_process_group()
+
+
+def test_max_and_sum_over_two_ranks_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+    res = sorted(q.get(timeout=5) for _ in range(2))
+    assert all(p.exitcode == 0 for p in procs)
+    assert [r[1] for r in res] == [3.0, 3.0]
+    assert [r[2] for r in res] == [3.0, 3.0]
+
+
+def test_reference_arm_nonzero_rank_exits_quietly(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_contract_line(monkeypatch, capsys):
+    monkeypatch.setattr(bench, "oracle_prefill_sample", lambda budget, seed=0: (2e9, 0.5, "s"))
+    assert bench.main(["--impl", "reference", "--steps", "2", "--warmup", "3"]) == 0
+    line = json.loads(capsys.readouterr().out.strip())
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "dtype", "config", "cpu_baseline", "e2e"):
+        assert key in line
+    assert line["impl"] == "reference"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert abs(line["value"] - 2e9 / 0.5 / 1e12) < 1e-12
