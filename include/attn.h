@@ -163,6 +163,32 @@ int attn_decode(const void* Q, const void* K, const void* V, const int* kv_lens,
                 int num_splits, float* O_part, float* LSE_part,
                 void* O, float* LSE, void* stream);
 
+/*
+ * attn_decode_noalloc - attn_decode for callers that cannot allocate.
+ *
+ * No counterpart in the pages: this is a convenience of this library. It is
+ * for callers that have no way to provide the partial buffers attn_decode
+ * needs: a serving runtime or plugin host that owns all device memory
+ * through its own fixed pool, a latency-critical token loop in which a
+ * cudaMalloc / cudaFree could block and synchronise the device, or plain C
+ * code that holds only the tensors it was handed.
+ *
+ * Same arguments and results as attn_decode minus O_part / LSE_part: the
+ * partials live in a fixed 32 MiB array inside the library (8 Mi floats),
+ * held on every GPU that loads the library until the process exits. The call
+ * allocates and frees nothing.
+ *   - Limit: B*Hq*S*(d + 1) floats must fit in 8 Mi floats (S the resolved
+ *     split count); larger calls return ATTN_ERR_WORKSPACE and launch nothing.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share the array; calls whose kernels overlap on
+ *     the GPU (unordered streams) race on it. Nothing in it needs clearing:
+ *     each call writes every partial it reads.
+ */
+int attn_decode_noalloc(const void* Q, const void* K, const void* V, const int* kv_lens,
+                        int B, int Hq, int Hkv, int Lk_max, int d, float scale,
+                        int num_splits, void* O, float* LSE, void* stream);
+
 /* Static text for a status code (never NULL). */
 const char* attn_status_string(int status);
 

@@ -42,6 +42,8 @@ SIGNATURES = {
                                                                      _c_void_p]),
     "attn_combine": (_c_int, [_c_void_p] * 2 + [_c_int] * 4 + [_c_void_p] * 3),
     "attn_decode": (_c_int, [_c_void_p] * 4 + [_c_int] * 5 + [_c_float, _c_int] + [_c_void_p] * 5),
+    "attn_decode_noalloc": (_c_int, [_c_void_p] * 4 + [_c_int] * 5 + [_c_float, _c_int] +
+                            [_c_void_p] * 3),
     "attn_status_string": (ctypes.c_char_p, [_c_int]),
     "attn_device_status": (_c_int, [_c_void_p]),
     "attn_version": (_c_int, []),
@@ -208,6 +210,29 @@ def decode(q, k, v, kv_lens=None, scale=None, num_splits=0, o_part=None, lse_par
                            float(scale), S, _ptr(o_part), _ptr(lse_part), _ptr(out), _ptr(lse),
                            _stream())
     _check(st, "attn_decode")
+    return out, lse
+
+
+def decode_noalloc(q, k, v, kv_lens=None, scale=None, num_splits=0, out=None, lse=None):
+    """Split-K decode + combine with the partials kept in the library's own
+    fixed device array (for callers that cannot allocate). Outputs are still
+    caller tensors; see attn_decode_noalloc in include/attn.h for the limit."""
+    _req(q, "q", torch.bfloat16, 3)
+    _req(k, "k", torch.bfloat16, 4)
+    _req(v, "v", torch.bfloat16, 4)
+    if kv_lens is not None:
+        _req(kv_lens, "kv_lens", torch.int32, 1)
+    B, Hq, d = q.shape
+    Hkv, Lk_max = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    st = lib().attn_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_lens), B, Hq, Hkv, Lk_max,
+                                   d, float(scale), num_splits, _ptr(out), _ptr(lse), _stream())
+    _check(st, "attn_decode_noalloc")
     return out, lse
 
 
