@@ -154,6 +154,7 @@ int attn_prefill_ex(const void* Q, const void* K, const void* V, void* O, float*
     L.p.G = Hq / Hkv;
     L.p.scale_log2 = scale * kLog2e;
     L.p.causal = causal ? 1 : 0;
+    L.p.pair_heads = (L.p.G % 2 == 0) ? 1 : 0;
     L.p.status = status_ptr();
     if (!L.p.status) return ATTN_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -37,6 +37,8 @@ struct PrefillParams {
     int B, Hq, Hkv, Lq, Lk, G;
     float scale_log2;         // softmax scale * log2(e)
     int causal;
+    int pair_heads;           // tcgen05 kernel: a CTA's two Q tiles are two query
+                              // heads of one KV group (1) or two row blocks (0)
     int* status;
 };
 

@@ -14,7 +14,7 @@ from tests.parity import assert_lse_close, assert_o_close
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = ["mma_sync"]
+IMPLS = ["tcgen05", "mma_sync"]
 
 
 @pytest.fixture(scope="module")
