@@ -9,18 +9,24 @@
 // the softmax of two Q sub-tiles in two separate warp groups. That page puts
 // the accumulator rescaling in a third group because TMEM reads block; here
 // the rescale is conditional (it runs only when a row max grows by more than
-// 2^8) and is done by the softmax group itself, so a third group would idle.
+// 2^8, which after the first KV tile is rare) and the softmax group does it.
 //
 // CTA = two 128-row Q tiles that share one KV head: either two consecutive
 // row blocks of one head (MHA) or the same row block of two query heads of a
-// GQA group. Per KV step j:
-//   TMA warp : K_j, V_j -> 3-slot shared-memory ring (128-byte swizzle)
-//   MMA warp : S_t = Q_t K_j^T into TMEM (t = 0, 1), then O_t += P_t V_j
+// GQA group. Tensor memory (512 columns): S_0, S_1 (128 fp32 columns each),
+// O_0, O_1 (d columns each). P_t (bf16, two keys per column) is written over
+// the upper half of S_t, and the PV product reads it straight from tensor
+// memory, so per KV step shared memory only carries Q K^T's operands, V and
+// the TMA writes.
+//
+// Per KV step j, for each tile t (the two tiles alternate on the tensor core):
+//   TMA warp : K_j, V_j -> 5-slot shared-memory ring (128-byte swizzle)
+//   MMA warp : O_t += P_t V_j (A from TMEM), then S_t = Q_t K_{j+1}^T
 //   softmax t: S_t (TMEM) -> registers, row max, p = 2^(x - m), row sum,
-//              P_t as bf16 into shared memory, O_t rescale in TMEM if needed
-// One thread owns one query row (TMEM lane = row), so row reductions need no
-// shuffles. Tensor memory: S_0, S_1 (128 fp32 columns each), O_0, O_1
-// (d columns each) out of 512.
+//              P_t (bf16) -> TMEM, O_t rescale in TMEM if needed
+// The commit that signals S_t^{j+1} also covers the PV product issued before
+// it, so when the softmax sees S_t^{j+1}, O_t is final for step j. One thread
+// owns one query row (TMEM lane = row): row reductions need no shuffles.
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
@@ -29,15 +35,19 @@ namespace attn {
 
 namespace {
 
-constexpr int kTcThreads = 384;                 // 12 warps
+constexpr int kTcThreads = 384;                 // 12 warps = 3 warpgroups
 constexpr int kSoftmaxWarp0 = 4;                // warps 4..7: tile 0, 8..11: tile 1
+// Register split (setmaxnreg, per warpgroup): launch 168 x 384 = 64512;
+// producer/MMA group 80 x 128 + two softmax groups 192 x 256 = 59392.
+constexpr int kRegsCtl = 80;
+constexpr int kRegsSoftmax = 192;
 constexpr float kRescaleThreshold = 8.0f;       // log2 units: rescale when max grows > 2^8
 constexpr uint32_t kTileBytes = 128 * 128;      // one 128-row x 128-byte swizzled box
 
 template <int D>
 struct TcCfg {
     static constexpr int kBoxes = D / 64;                   // 64-element boxes per row
-    static constexpr int kStages = D == 128 ? 3 : 6;        // K/V ring slots
+    static constexpr int kStages = D == 128 ? 5 : 10;       // K/V ring slots
     static constexpr uint32_t kSlotBytes = kBoxes * kTileBytes;
 };
 
@@ -45,12 +55,10 @@ template <int D>
 struct TcSmem {
     alignas(1024) uint8_t q[2][TcCfg<D>::kBoxes][kTileBytes];
     alignas(1024) uint8_t kv[TcCfg<D>::kStages][TcCfg<D>::kBoxes][kTileBytes];
-    alignas(1024) uint8_t p[2][2][kTileBytes];   // P_t: keys 0..63, 64..127
     uint64_t bar_q;
     uint64_t kv_full[TcCfg<D>::kStages];
     uint64_t kv_empty[TcCfg<D>::kStages];
     uint64_t s_full[2];
-    uint64_t s_free[2];
     uint64_t p_full[2];
     uint64_t o_done[2];
     uint64_t mma_fin;
@@ -99,15 +107,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int n_rb = (p.Lq + rows_per_item - 1) / rows_per_item;
     const int rb = n_rb - 1 - int(blockIdx.x) / n_hb;
     const int hb = int(blockIdx.x) % n_hb;
-    TileInfo tile[2];
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        tile[t].head = pair_heads ? 2 * hb + t : hb;
-        tile[t].row0 = pair_heads ? rb * 128 : rb * 256 + t * 128;
-        tile[t].n = kv_tiles_for(tile[t].row0, p.Lq, p.Lk, CAUSAL);
-    }
-    const int kvh = tile[0].head / p.G;
-    const int n = max(tile[0].n, tile[1].n);
+    const int head0 = pair_heads ? 2 * hb : hb;
+    const int head1 = pair_heads ? 2 * hb + 1 : hb;
+    const int row00 = pair_heads ? rb * 128 : rb * 256;
+    const int row01 = pair_heads ? rb * 128 : rb * 256 + 128;
+    const int n0 = kv_tiles_for(row00, p.Lq, p.Lk, CAUSAL);
+    const int n1 = kv_tiles_for(row01, p.Lq, p.Lk, CAUSAL);
+    const int kvh = head0 / p.G;
+    const int n = max(n0, n1);
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.bar_q, 1);
@@ -117,7 +124,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&sm.s_full[t], 1);
-            mbar_init(&sm.s_free[t], 4);
             mbar_init(&sm.p_full[t], 4);
             mbar_init(&sm.o_done[t], 1);
         }
@@ -136,7 +142,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     volatile int* abort = &sm.abort;
     int issued = 0;   // TMA loads issued (producer thread)
 
-    if (warp == 0) {
+    if (warp < kSoftmaxWarp0) {
+      // control warpgroup: TMA producer (warp 0) and MMA issuer (warp 1)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+      if (warp == 0) {
         // ============================================== TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
@@ -144,31 +153,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_prefetch_desc(&tmV);
             mbar_arrive_expect_tx(&sm.bar_q, 2u * Cfg::kBoxes * kTileBytes);
 #pragma unroll
-            for (int t = 0; t < 2; ++t)
-#pragma unroll
-                for (int bx = 0; bx < Cfg::kBoxes; ++bx)
-                    tma_load_3d(sm.q[t][bx], &tmQ, &sm.bar_q, bx * 64, tile[t].row0,
-                                b * p.Hq + tile[t].head);
+            for (int bx = 0; bx < Cfg::kBoxes; ++bx) {
+                tma_load_3d(sm.q[0][bx], &tmQ, &sm.bar_q, bx * 64, row00, b * p.Hq + head0);
+                tma_load_3d(sm.q[1][bx], &tmQ, &sm.bar_q, bx * 64, row01, b * p.Hq + head1);
+            }
             const int z = b * p.Hkv + kvh;
-            int u = 0;
-            bool ok = true;
-            auto load = [&](int j, bool is_k) {
+            // ring order = consumption order: K_0, V_0, K_1, V_1, ...
+            for (int u = 0; u < 2 * n; ++u) {
                 const int slot = u % NS;
                 if (u >= NS && !mbar_wait(&sm.kv_empty[slot], ((u / NS) - 1) & 1, abort, p.status))
-                    return false;
+                    break;
                 mbar_arrive_expect_tx(&sm.kv_full[slot], Cfg::kSlotBytes);
+                const CUtensorMap* map = (u & 1) ? &tmV : &tmK;
 #pragma unroll
                 for (int bx = 0; bx < Cfg::kBoxes; ++bx)
-                    tma_load_3d(sm.kv[slot][bx], is_k ? &tmK : &tmV, &sm.kv_full[slot], bx * 64,
-                                j * 128, z);
-                ++u;
-                issued = u;
-                return true;
-            };
-            if (n > 0) ok = load(0, true);
-            for (int j = 0; ok && j < n; ++j) {
-                if (j + 1 < n) ok = load(j + 1, true);
-                if (ok) ok = load(j, false);
+                    tma_load_3d(sm.kv[slot][bx], map, &sm.kv_full[slot], bx * 64, (u >> 1) * 128, z);
+                issued = u + 1;
             }
         }
     } else if (warp == 1) {
@@ -176,128 +176,146 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_bf16(128, 128, 0);
             constexpr uint32_t idO = tc::idesc_bf16(128, D, 1);
-            const uint32_t tS[2] = {tbase, tbase + 128};
-            const uint32_t tO[2] = {tbase + 256, tbase + 256 + D};
+            const int nt[2] = {n0, n1};
             bool ok = mbar_wait(&sm.bar_q, 0, abort, p.status);
             tc::fence_after_sync();
-            int u = 0;
-            auto acquire = [&](int& slot) {
-                slot = u % NS;
-                if (!mbar_wait(&sm.kv_full[slot], (u / NS) & 1, abort, p.status)) return false;
+            int u = 0;   // next ring entry to consume
+            auto acquire = [&]() {
+                const int slot = u % NS;
+                if (!mbar_wait(&sm.kv_full[slot], (u / NS) & 1, abort, p.status)) return -1;
                 tc::fence_after_sync();
-                return true;
+                return slot;
             };
             auto release = [&](int slot) {
                 tc::commit(&sm.kv_empty[slot]);
                 ++u;
             };
+            // Descriptors are built once; a K-step or ring slot only moves the
+            // start-address field (16-byte units, 14 bits: every shared
+            // address here is below 256 KB, so the field cannot overflow).
+            const uint64_t qdesc0 = tc::sdesc_sw128(smem_u32(sm.q[0][0]), 16, 1024);
+            const uint64_t qdesc1 = tc::sdesc_sw128(smem_u32(sm.q[1][0]), 16, 1024);
+            const uint64_t kdesc0 = tc::sdesc_sw128(smem_u32(sm.kv[0][0]), 16, 1024);
+            const uint64_t vdesc0 = tc::sdesc_sw128(smem_u32(sm.kv[0][0]), kTileBytes, 1024);
+            constexpr uint32_t kSlotStep = Cfg::kSlotBytes >> 4;
             auto issue_s = [&](int t, int slot) {
-                const uint32_t qa = smem_u32(sm.q[t][0]);
-                const uint32_t ka = smem_u32(sm.kv[slot][0]);
+                const uint64_t a0 = t ? qdesc1 : qdesc0;
+                const uint64_t b0 = kdesc0 + uint64_t(uint32_t(slot) * kSlotStep);
+                const uint32_t d = tbase + t * 128;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t offb = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-                    tc::mma_bf16_ss(tS[t], tc::sdesc_sw128(qa + offb, 16, 1024),
-                                    tc::sdesc_sw128(ka + offb, 16, 1024), idS, kk > 0);
+                    const uint32_t o = ((kk >> 2) * kTileBytes + (kk & 3) * 32) >> 4;
+                    tc::mma_bf16_ss(d, a0 + o, b0 + o, idS, kk > 0);
                 }
-                tc::commit(&sm.s_full[t]);
             };
             auto issue_pv = [&](int t, int slot, int j) {
-                const uint32_t pa = smem_u32(sm.p[t][0]);
-                const uint32_t va = smem_u32(sm.kv[slot][0]);
+                const uint64_t b0 = vdesc0 + uint64_t(uint32_t(slot) * kSlotStep);
+                const uint32_t tP = tbase + t * 128 + 64;
+                const uint32_t d = tbase + 256 + t * D;
+                const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t offa = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-                    tc::mma_bf16_ss(tO[t], tc::sdesc_sw128(pa + offa, 16, 1024),
-                                    tc::sdesc_sw128(va + kk * 2048, kTileBytes, 1024), idO,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc::commit(&sm.o_done[t]);
+                for (int kk = 0; kk < 8; ++kk)
+                    tc::mma_bf16_ts(d, tP + kk * 8, b0 + uint32_t(kk * (2048 >> 4)), idO,
+                                    kk > 0 ? 1u : acc0);
             };
-            int slot = 0;
             if (ok && n > 0) {
-                ok = acquire(slot);
+                const int ks = acquire();
+                ok = ks >= 0;
                 if (ok) {
                     for (int t = 0; t < 2; ++t)
-                        if (tile[t].n > 0) issue_s(t, slot);
-                    release(slot);
+                        if (nt[t] > 0) {
+                            issue_s(t, ks);
+                            tc::commit(&sm.s_full[t]);
+                        }
+                    release(ks);
                 }
             }
             for (int j = 0; ok && j < n; ++j) {
-                if (j + 1 < n) {
-                    ok = acquire(slot);
-                    if (!ok) break;
-                    for (int t = 0; ok && t < 2; ++t) {
-                        if (j + 1 < tile[t].n) {
-                            ok = mbar_wait(&sm.s_free[t], j & 1, abort, p.status);
-                            tc::fence_after_sync();
-                            if (ok) issue_s(t, slot);
-                        }
-                    }
-                    if (!ok) break;
-                    release(slot);
-                }
-                ok = acquire(slot);
-                if (!ok) break;
+                const int vs = acquire();           // V_j
+                if (vs < 0) break;
+                int ks = -1;
                 for (int t = 0; ok && t < 2; ++t) {
-                    if (j < tile[t].n) {
-                        ok = mbar_wait(&sm.p_full[t], j & 1, abort, p.status);
-                        tc::fence_after_sync();
-                        if (ok) issue_pv(t, slot, j);
+                    if (j >= nt[t]) continue;
+                    ok = mbar_wait(&sm.p_full[t], j & 1, abort, p.status);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    issue_pv(t, vs, j);
+                    if (j + 1 < nt[t]) {
+                        if (ks < 0) {
+                            ++u;                    // K_{j+1} follows V_j in the ring
+                            ks = acquire();
+                            --u;
+                            if (ks < 0) { ok = false; break; }
+                        }
+                        issue_s(t, ks);
+                        tc::commit(&sm.s_full[t]);
+                    } else {
+                        tc::commit(&sm.o_done[t]);
                     }
                 }
                 if (!ok) break;
-                release(slot);
+                release(vs);
+                if (j + 1 < n) {
+                    // every tile that needs K_{j+1} has consumed it by now; a
+                    // tile that does not (the shorter causal tile) never waits
+                    if (ks < 0) ks = acquire();
+                    if (ks < 0) break;
+                    release(ks);
+                }
             }
             // every MMA this thread issued completes before the CTA ends
             tc::commit(&sm.mma_fin);
             volatile int never = 0;
             mbar_wait(&sm.mma_fin, 0, &never, p.status);
         }
-    } else if (warp >= kSoftmaxWarp0) {
+      }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         // ============================================== softmax groups
         const int t = (warp - kSoftmaxWarp0) >> 2;
         const int q4 = warp & 3;                  // TMEM lane quadrant of this warp
         const int r = q4 * 32 + lane;             // row within the tile
-        const TileInfo ti = tile[t];
-        const int row = ti.row0 + r;
+        const int head = t ? head1 : head0;
+        const int row0 = t ? row01 : row00;
+        const int ntile = t ? n1 : n0;
+        const int row = row0 + r;
         const int i_al = row + off;               // bottom-right aligned row index
         const uint32_t lane_off = uint32_t(q4 * 32) << 16;
         const uint32_t tS = tbase + t * 128 + lane_off;
+        const uint32_t tP = tS + 64;
         const uint32_t tO = tbase + 256 + t * D + lane_off;
         const float sl2 = p.scale_log2;
-        const float slope_l2 = ALIBI ? p.slopes[ti.head] * kLog2e : 0.f;
-        uint8_t* prow = &sm.p[t][0][0];
+        const float slope_l2 = ALIBI ? p.slopes[head] * kLog2e : 0.f;
 
         float m = -INFINITY;   // reference max (log2 domain)
         float l = 0.f;
         bool ok = true;
-        for (int j = 0; j < ti.n; ++j) {
+        for (int j = 0; j < ntile; ++j) {
             ok = mbar_wait(&sm.s_full[t], j & 1, abort, p.status);
             if (!ok) break;
             tc::fence_after_sync();
             float s[128];
+            {
+                uint32_t rr[128];
+                tc::tmem_ld_32x32b_x128(tS, rr);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t rr[32];
-                tc::tmem_ld_32x32b_x32(tS + c * 32, rr);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(rr[i]);
+                for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(rr[i]);
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.s_free[t]);
-
             const int k0 = j * 128;
             const bool need_mask =
-                (k0 + 128 > p.Lk) || (CAUSAL && k0 + 127 > ti.row0 + q4 * 32 + off);
+                (k0 + 128 > p.Lk) || (CAUSAL && k0 + 127 > row0 + q4 * 32 + off);
             // x = s * scale (log2 domain) + bias, masked; on unmasked tiles
             // without bias the scale is folded into the exp's FMA below
             const bool fast = !need_mask && !ALIBI && sl2 > 0.f;
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (fast) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
+                for (int c = 0; c < 128; c += 8) {
+                    mx4[0] = max3(mx4[0], s[c], s[c + 1]);
+                    mx4[1] = max3(mx4[1], s[c + 2], s[c + 3]);
+                    mx4[2] = max3(mx4[2], s[c + 4], s[c + 5]);
+                    mx4[3] = max3(mx4[3], s[c + 6], s[c + 7]);
+                }
             } else {
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
@@ -312,7 +330,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mx4[c & 3] = fmaxf(mx4[c & 3], x);
                 }
             }
-            float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            float mx = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
             if (fast) mx *= sl2;
             // conditional repair: move the reference max only when the row max
             // exceeds it by more than the threshold (or it is still unset)
@@ -321,72 +339,67 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool rescale = (j > 0) && (m != -INFINITY) && (m_new != m);
             const float corr = rescale ? ex2(m - m_new) : 1.f;
             const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-            if (fast) {
+            // p = 2^(x - m) as one packed FMA per key pair (x = s * scale on
+            // the fast path; s already holds x otherwise, times exactly 1),
+            // row sum with packed adds, and P_t (bf16) over the upper half of
+            // S_t in tensor memory, 64 keys at a time (S_t is in registers)
+            const float mul = fast ? sl2 : 1.f;
+            const uint64_t mul2 = f2_pack(mul, mul);
+            const uint64_t neg2 = f2_pack(-m_use, -m_use);
+            uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const float pv = ex2(fmaf(s[c], sl2, -m_use));
-                    s[c] = pv;
-                    rs4[c & 3] += pv;
-                }
-            } else {
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const float pv = ex2(s[c] - m_use);
-                    s[c] = pv;
-                    rs4[c & 3] += pv;
+                for (int c2 = 0; c2 < 32; ++c2) {
+                    const int c = h * 64 + 2 * c2;
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), mul2, neg2), x0, x1);
+                    const float p0 = ex2(x0);
+                    const float p1 = ex2(x1);
+                    sum2[c2 & 1] = f2_add(sum2[c2 & 1], f2_pack(p0, p1));
+                    pk[c2] = pack_bf16(p0, p1);
                 }
+                tc::tmem_st_32x32b_x32(tP + h * 32, pk);
             }
-            const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
-            l = l * corr + rs;
+            float sa, sb, sc, sd;
+            f2_unpack(sum2[0], sa, sb);
+            f2_unpack(sum2[1], sc, sd);
+            l = l * corr + ((sa + sb) + (sc + sd));
             m = m_new;
-
-            // P_t and O_t are free once PV of the previous step is done
-            if (j > 0) {
-                ok = mbar_wait(&sm.o_done[t], (j - 1) & 1, abort, p.status);
-                if (!ok) break;
-                tc::fence_after_sync();
-            }
-#pragma unroll
-            for (int c16 = 0; c16 < 16; ++c16) {
-                uint4 w;
-                w.x = pack_bf16(s[c16 * 8 + 0], s[c16 * 8 + 1]);
-                w.y = pack_bf16(s[c16 * 8 + 2], s[c16 * 8 + 3]);
-                w.z = pack_bf16(s[c16 * 8 + 4], s[c16 * 8 + 5]);
-                w.w = pack_bf16(s[c16 * 8 + 6], s[c16 * 8 + 7]);
-                *reinterpret_cast<uint4*>(prow + (c16 >> 3) * kTileBytes +
-                                          sw128_off(r, c16 & 7)) = w;
-            }
-            fence_proxy_async_smem();
+            // O_t holds step j-1's result (the commit that signalled S_t^j
+            // covers the PV issued before it): repair it if the max moved
             if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t rr[32];
                     tc::tmem_ld_32x32b_x32(tO + c * 32, rr);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * corr);
+                    for (int i = 0; i < 32; ++i)
+                        rr[i] = __float_as_uint(__uint_as_float(rr[i]) * corr);
                     tc::tmem_st_32x32b_x32(tO + c * 32, rr);
                 }
-                tc::tmem_wait_st();
             }
+            tc::tmem_wait_st();
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.p_full[t]);
         }
 
         // ---------------------------------------------------- epilogue
-        if (ok && ti.n > 0) {
-            ok = mbar_wait(&sm.o_done[t], (ti.n - 1) & 1, abort, p.status);
+        if (ok && ntile > 0) {
+            ok = mbar_wait(&sm.o_done[t], 0, abort, p.status);
             tc::fence_after_sync();
         }
         if (ok && !*abort) {
             const bool valid = row < p.Lq;
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16* orow = p.O + ((size_t(b) * p.Hq + ti.head) * p.Lq + (valid ? row : 0)) * D;
+            __nv_bfloat16* orow =
+                p.O + ((size_t(b) * p.Hq + head) * p.Lq + (valid ? row : 0)) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t rr[32];
-                if (ti.n > 0) {
+                if (ntile > 0) {
                     tc::tmem_ld_32x32b_x32(tO + c * 32, rr);
                 } else {
 #pragma unroll
@@ -396,16 +409,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int v8 = 0; v8 < 4; ++v8) {
                         uint4 w;
-                        w.x = pack_bf16(__uint_as_float(rr[v8 * 8 + 0]) * inv, __uint_as_float(rr[v8 * 8 + 1]) * inv);
-                        w.y = pack_bf16(__uint_as_float(rr[v8 * 8 + 2]) * inv, __uint_as_float(rr[v8 * 8 + 3]) * inv);
-                        w.z = pack_bf16(__uint_as_float(rr[v8 * 8 + 4]) * inv, __uint_as_float(rr[v8 * 8 + 5]) * inv);
-                        w.w = pack_bf16(__uint_as_float(rr[v8 * 8 + 6]) * inv, __uint_as_float(rr[v8 * 8 + 7]) * inv);
+                        w.x = pack_bf16(__uint_as_float(rr[v8 * 8 + 0]) * inv,
+                                        __uint_as_float(rr[v8 * 8 + 1]) * inv);
+                        w.y = pack_bf16(__uint_as_float(rr[v8 * 8 + 2]) * inv,
+                                        __uint_as_float(rr[v8 * 8 + 3]) * inv);
+                        w.z = pack_bf16(__uint_as_float(rr[v8 * 8 + 4]) * inv,
+                                        __uint_as_float(rr[v8 * 8 + 5]) * inv);
+                        w.w = pack_bf16(__uint_as_float(rr[v8 * 8 + 6]) * inv,
+                                        __uint_as_float(rr[v8 * 8 + 7]) * inv);
                         *reinterpret_cast<uint4*>(orow + c * 32 + v8 * 8) = w;
                     }
                 }
             }
             if (valid && p.LSE)
-                p.LSE[(size_t(b) * p.Hq + ti.head) * p.Lq + row] =
+                p.LSE[(size_t(b) * p.Hq + head) * p.Lq + row] =
                     l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
         }
         tc::fence_before_sync();
