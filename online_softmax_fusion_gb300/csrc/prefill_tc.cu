@@ -173,7 +173,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (warp == 1) {
         // ============================================== MMA issuer
-        if (lane == 0) {
+        // (the whole warp runs the loop; one elected lane issues)
+        {
             constexpr uint32_t idS = tc::idesc_bf16(128, 128, 0);
             constexpr uint32_t idO = tc::idesc_bf16(128, D, 1);
             const int nt[2] = {n0, n1};
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 return slot;
             };
             auto release = [&](int slot) {
-                tc::commit(&sm.kv_empty[slot]);
+                tc::commit_warp(&sm.kv_empty[slot]);
                 ++u;
             };
             // Descriptors are built once; a K-step or ring slot only moves the
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t o = ((kk >> 2) * kTileBytes + (kk & 3) * 32) >> 4;
-                    tc::mma_bf16_ss(d, a0 + o, b0 + o, idS, kk > 0);
+                    tc::mma_bf16_ss_warp(d, a0 + o, b0 + o, idS, kk > 0);
                 }
             };
             auto issue_pv = [&](int t, int slot, int j) {
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_bf16_ts(d, tP + kk * 8, b0 + uint32_t(kk * (2048 >> 4)), idO,
+                    tc::mma_bf16_ts_warp(d, tP + kk * 8, b0 + uint32_t(kk * (2048 >> 4)), idO,
                                     kk > 0 ? 1u : acc0);
             };
             if (ok && n > 0) {
@@ -225,7 +226,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int t = 0; t < 2; ++t)
                         if (nt[t] > 0) {
                             issue_s(t, ks);
-                            tc::commit(&sm.s_full[t]);
+                            tc::commit_warp(&sm.s_full[t]);
                         }
                     release(ks);
                 }
@@ -248,9 +249,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             if (ks < 0) { ok = false; break; }
                         }
                         issue_s(t, ks);
-                        tc::commit(&sm.s_full[t]);
+                        tc::commit_warp(&sm.s_full[t]);
                     } else {
-                        tc::commit(&sm.o_done[t]);
+                        tc::commit_warp(&sm.o_done[t]);
                     }
                 }
                 if (!ok) break;
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             // every MMA this thread issued completes before the CTA ends
-            tc::commit(&sm.mma_fin);
+            tc::commit_warp(&sm.mma_fin);
             volatile int never = 0;
             mbar_wait(&sm.mma_fin, 0, &never, p.status);
         }
