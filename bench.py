@@ -115,10 +115,12 @@ def recorded_traffic(kernel: str, relpath: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling in the background."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle sampling in the background; stop() keeps
+    the samples whose timestamps fall inside the timed region."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
@@ -131,37 +133,63 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         return self
 
-    def stop(self):
+    @staticmethod
+    def _epoch(ts: str):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(ts.strip(), fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    @classmethod
+    def summarize(cls, lines, t0=None, t1=None):
+        rows = []
+        for line in lines:
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 10:
+                continue
+            ts = cls._epoch(p[0])
+            rows.append((ts, p))
+        inside = [p for ts, p in rows
+                  if t0 is None or (ts is not None and t0 - 0.025 <= ts <= t1 + 0.025)]
+        use = inside if inside else [p for _, p in rows]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(r[2]) for r in use) if v is not None]
+        mx = [v for v in (num(r[3]) for r in use) if v is not None]
+        pw = [v for v in (num(r[4]) for r in use) if v is not None]
+        reasons = sorted({cls.REASONS[i] for r in use for i in range(4) if r[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples_in_region": len(inside), "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+    def stop(self, t0=None, t1=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
                     "samples": 0}
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                p = [x.strip() for x in line.split(",")]
-                if len(p) >= 9:
-                    rows.append(p)
+            lines = f.readlines()
         os.unlink(self.path)
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
-        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows),
-                "power_w_max": max(pw) if pw else None}
+        return self.summarize(lines, t0, t1)
 
 
 def dist_env():
@@ -190,6 +218,63 @@ def sum_over_ranks(value: float, world: int, device=None) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def time_launches(fn, steps, warmup, stream):
+    """Mean CUDA-event time (ms) of fn() over `steps` launches after warm-up."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def measure_other_workloads(attn, W, dev, peaks):
+    """The remaining workloads, each timed on its own (inputs > L2 except the
+    smallest sweep lengths, which are noted): the causal GQA + ALiBi prefill
+    sweep over L and the long-context outlier decode with 64 splits."""
+    import torch
+    stream = torch.cuda.current_stream()
+    sweep = []
+    for L in W.GQA_SWEEP_LENGTHS:
+        cfg = W.gqa_sweep_config(L)
+        inp = W.make_prefill_inputs(cfg, dev)
+        O = torch.empty_like(inp["q"])
+        LSE = torch.empty((cfg.B, cfg.Hq, cfg.Lq), dtype=torch.float32, device=dev)
+        fn = lambda: attn.prefill(inp["q"], inp["k"], inp["v"], causal=True, scale=cfg.scale,  # noqa: E731
+                                  alibi_slopes=inp["alibi_slopes"], out=O, lse=LSE)
+        ms = time_launches(fn, 10 if L <= 8192 else 4, 3, stream)
+        fl = prefill_flops(cfg.B, cfg.Hq, cfg.Lq, cfg.Lk, cfg.d, True)
+        tf = fl / (ms * 1e-3) / 1e12
+        in_bytes = (inp["q"].numel() + inp["k"].numel() + inp["v"].numel()) * 2
+        sweep.append({"L": L, "ms": ms, "tflops": tf, "frac": tf / peaks["bf16_tflops"],
+                      "inputs_exceed_l2": in_bytes > 129e6})
+        del inp, O, LSE
+    dc = W.DECODE_CONFIGS["decode_long_outlier"]
+    din = W.make_decode_inputs(dc, dev)
+    S = attn.resolve_splits(dc.B, dc.Hkv, dc.Lk_max, dc.d, dc.num_splits)
+    Op = torch.empty((dc.B, dc.Hq, S, dc.d), dtype=torch.float32, device=dev)
+    Lp = torch.empty((dc.B, dc.Hq, S), dtype=torch.float32, device=dev)
+    Od = torch.empty((dc.B, dc.Hq, dc.d), dtype=torch.bfloat16, device=dev)
+    Ld = torch.empty((dc.B, dc.Hq), dtype=torch.float32, device=dev)
+    t_dec = time_launches(lambda: attn.decode_splitk(din["q"], din["k"], din["v"], din["kv_lens"],
+                                                     scale=dc.scale, num_splits=S, o_part=Op,
+                                                     lse_part=Lp), 10, 3, stream)
+    t_cmb = time_launches(lambda: attn.combine(Op, Lp, out=Od, lse=Ld), 10, 3, stream)
+    kvb = decode_kv_bytes(dc.Hkv, din["kv_lens"].cpu().tolist(), dc.d)
+    gbs = kvb / (t_dec * 1e-3) / 1e9
+    long_dec = {"workload": dc.name, "splits": S, "ms_decode": t_dec, "ms_combine": t_cmb,
+                "kv_gbs": gbs, "path_gbs": kvb / ((t_dec + t_cmb) * 1e-3) / 1e9,
+                "frac": gbs / peaks["hbm_gbs"], "kv_bytes": kvb}
+    del din, Op, Lp, Od, Ld
+    return {"prefill_gqa_alibi_sweep": sweep, "decode_long_outlier": long_dec}
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -282,112 +367,141 @@ def run_ours(args):
     import workloads as W
     attn.lib()
     peaks, peak_src = load_peaks()
+    do_p = args.kernel in ("all", "prefill")
+    do_d = args.kernel in ("all", "decode")
 
     pc = W.PREFILL_CONFIGS[PREFILL_WORKLOAD]
     dc = W.DECODE_CONFIGS[DECODE_WORKLOAD]
-    pin = W.make_prefill_inputs(pc, dev)
-    din = W.make_decode_inputs(dc, dev)
-    q, k, v = pin["q"], pin["k"], pin["v"]
-    O = torch.empty_like(q)
-    LSE = torch.empty((pc.B, pc.Hq, pc.Lq), dtype=torch.float32, device=dev)
-    S = attn.resolve_splits(dc.B, dc.Hkv, dc.Lk_max, dc.d, dc.num_splits)
-    Op = torch.empty((dc.B, dc.Hq, S, dc.d), dtype=torch.float32, device=dev)
-    Lp = torch.empty((dc.B, dc.Hq, S), dtype=torch.float32, device=dev)
-    Od = torch.empty((dc.B, dc.Hq, dc.d), dtype=torch.bfloat16, device=dev)
-    Ld = torch.empty((dc.B, dc.Hq), dtype=torch.float32, device=dev)
-    kv_lens = din["kv_lens"]
+    if args.small:
+        # same distribution, a quarter of the batch: ~2 GB of K/V on the device
+        dc = W.DecodeConfig(dc.name + "_b16", B=16, Hq=dc.Hq, Hkv=dc.Hkv, Lk_max=dc.Lk_max,
+                            d=dc.d, len_lo=dc.len_lo, len_hi=dc.len_hi, seed=dc.seed)
+    launches = []
+    if do_p:
+        pin = W.make_prefill_inputs(pc, dev)
+        q, k, v = pin["q"], pin["k"], pin["v"]
+        O = torch.empty_like(q)
+        LSE = torch.empty((pc.B, pc.Hq, pc.Lq), dtype=torch.float32, device=dev)
 
-    def prefill():
-        attn.prefill(q, k, v, causal=True, scale=pc.scale, out=O, lse=LSE)
+        def prefill():
+            attn.prefill(q, k, v, causal=True, scale=pc.scale, out=O, lse=LSE)
+        launches.append(("prefill", prefill))
+    if do_d:
+        din = W.make_decode_inputs(dc, dev)
+        S = attn.resolve_splits(dc.B, dc.Hkv, dc.Lk_max, dc.d, dc.num_splits)
+        Op = torch.empty((dc.B, dc.Hq, S, dc.d), dtype=torch.float32, device=dev)
+        Lp = torch.empty((dc.B, dc.Hq, S), dtype=torch.float32, device=dev)
+        Od = torch.empty((dc.B, dc.Hq, dc.d), dtype=torch.bfloat16, device=dev)
+        Ld = torch.empty((dc.B, dc.Hq), dtype=torch.float32, device=dev)
+        kv_lens = din["kv_lens"]
 
-    def decode_part():
-        attn.decode_splitk(din["q"], din["k"], din["v"], kv_lens, scale=dc.scale, num_splits=S,
-                           o_part=Op, lse_part=Lp)
+        def decode_part():
+            attn.decode_splitk(din["q"], din["k"], din["v"], kv_lens, scale=dc.scale,
+                               num_splits=S, o_part=Op, lse_part=Lp)
 
-    def combine_part():
-        attn.combine(Op, Lp, out=Od, lse=Ld)
+        def combine_part():
+            attn.combine(Op, Lp, out=Od, lse=Ld)
+        launches += [("decode", decode_part), ("combine", combine_part)]
 
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
-        prefill()
-        decode_part()
-        combine_part()
+        for _, fn in launches:
+            fn()
     torch.cuda.synchronize()
     assert attn.device_status() == 0, "device status after warm-up"
 
     clocks = ClockSampler(dev.index).start()
-    time.sleep(0.3)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    time.sleep(0.5)   # let nvidia-smi start sampling before the region opens
+    nl = len(launches)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
     start.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
-        prefill()
-        ev[i][1].record(stream)
-        decode_part()
-        ev[i][2].record(stream)
-        combine_part()
-        ev[i][3].record(stream)
+        for li, (_, fn) in enumerate(launches):
+            fn()
+            ev[i][li + 1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
+    t_wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-    clk = clocks.stop()
+    clk = clocks.stop(t_wall0, t_wall1)
     st = attn.device_status()
     assert st == 0, f"device status {st}"
 
-    total_ms = start.elapsed_time(end)
-    t_prefill = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps   # ms per launch
-    t_decode = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
-    t_combine = sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps
-    total_ms = max_over_ranks(total_ms, world, dev)
-    t_prefill_max = max_over_ranks(t_prefill, world, dev)
+    total_ms = max_over_ranks(start.elapsed_time(end), world, dev)
+    per = {}
+    for li, (name, _) in enumerate(launches):
+        per[name] = sum(e[li].elapsed_time(e[li + 1]) for e in ev) / args.steps  # ms per launch
 
     fl = prefill_flops(pc.B, pc.Hq, pc.Lq, pc.Lk, pc.d, True)
-    value = fl * world / (t_prefill_max * 1e-3) / 1e12            # whole job, TFLOP/s
-    achieved = fl / (t_prefill * 1e-3) / 1e12
-    lens = kv_lens.cpu().tolist()
-    kvb = decode_kv_bytes(dc.Hkv, lens, dc.d)
-    dec_gbs = kvb / (t_decode * 1e-3) / 1e9
-    dec_path_gbs = kvb / ((t_decode + t_combine) * 1e-3) / 1e9
+    value = achieved = None
+    if do_p:
+        t_prefill_max = max_over_ranks(per["prefill"], world, dev)
+        value = fl * world / (t_prefill_max * 1e-3) / 1e12            # whole job, TFLOP/s
+        achieved = fl / (per["prefill"] * 1e-3) / 1e12
+    decode_obj = None
+    kvb = None
+    if do_d:
+        lens = kv_lens.cpu().tolist()
+        kvb = decode_kv_bytes(dc.Hkv, lens, dc.d)
+        dec_gbs = kvb / (per["decode"] * 1e-3) / 1e9
+        dec_path_gbs = kvb / ((per["decode"] + per["combine"]) * 1e-3) / 1e9
+        dec_traffic = recorded_traffic("decode", "online_softmax_fusion_gb300/csrc/decode.cu")
+        decode_obj = {"metric": "KV GB/s (decode)", "value": dec_gbs * world, "unit": "GB/s",
+                      "path_value": dec_path_gbs * world, "ms_decode": per["decode"],
+                      "ms_combine": per["combine"], "workload": dc.name,
+                      "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
+                                   "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
+                                   "traffic": dec_traffic,
+                                   "peak_kind": f"{peak_src} copy bandwidth"}}
+        if not do_p:
+            value = dec_gbs * world
 
     # ----- e2e: host buffers through the public API, copies inside the region
-    hq = q.cpu().pin_memory()
-    hk = k.cpu().pin_memory()
-    hv = v.cpu().pin_memory()
-    ho = torch.empty(O.shape, dtype=O.dtype).pin_memory()
-    hl = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    e2e_steps = max(3, min(args.steps, 10))
+    e2e = None
+    if do_p:
+        hq = q.cpu().pin_memory()
+        hk = k.cpu().pin_memory()
+        hv = v.cpu().pin_memory()
+        ho = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+        hl = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        e2e_steps = max(3, min(args.steps, 10))
 
-    def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        attn.prefill(dq, dk, dv, causal=True, scale=pc.scale, out=O, lse=LSE)
-        ho.copy_(O, non_blocking=True)
-        hl.copy_(LSE, non_blocking=True)
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            attn.prefill(dq, dk, dv, causal=True, scale=pc.scale, out=O, lse=LSE)
+            ho.copy_(O, non_blocking=True)
+            hl.copy_(LSE, non_blocking=True)
 
-    e2e_step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
         e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
-    e2e_val = fl * world / (e2e_ms * 1e-3) / 1e12
-    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
-    d2h = ho.numel() * 2 + hl.numel() * 4
-    del hq, hk, hv, ho, hl, dq, dk, dv
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+        e2e = {"value": fl * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": (hq.numel() + hk.numel() + hv.numel()) * 2,
+               "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4, "ms_per_step": e2e_ms}
+        del hq, hk, hv, ho, hl, dq, dk, dv
 
-    out = None
+    others = None
+    if args.kernel == "all" and not args.no_other_workloads:
+        others = measure_other_workloads(attn, W, dev, peaks)
+
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
@@ -395,38 +509,40 @@ def run_ours(args):
             cpu = {"value": cfl / cdt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
                    "kind": "oracle", "sample": cdesc, "seconds": round(cdt, 2)}
         pk_t = peaks["bf16_tflops"]
-        traffic = recorded_traffic("prefill", "online_softmax_fusion_gb300/csrc/prefill_tc.cu")
-        dec_traffic = recorded_traffic("decode", "online_softmax_fusion_gb300/csrc/decode.cu")
+        roof = None
+        if do_p:
+            roof = {"bound": "tensor", "achieved": achieved, "peak": pk_t, "unit": "TFLOP/s",
+                    "frac": achieved / pk_t,
+                    "traffic": recorded_traffic("prefill",
+                                                "online_softmax_fusion_gb300/csrc/prefill_tc.cu"),
+                    "peak_kind": f"{peak_src} bf16 burst",
+                    "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                    "kernel": "prefill_tc_kernel", "ms_per_launch": per["prefill"]}
+        elif do_d:
+            roof = decode_obj["roofline"]
+        workload = {"all": f"{PREFILL_WORKLOAD} + {dc.name}", "prefill": PREFILL_WORKLOAD,
+                    "decode": dc.name}[args.kernel]
         out = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "metric": METRIC, "value": value,
+            "unit": "TFLOP/s" if do_p else "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": f"{PREFILL_WORKLOAD} + {DECODE_WORKLOAD}",
+            "config": {"workload": workload,
                        "prefill": {"B": pc.B, "H": pc.Hq, "L": pc.Lq, "d": pc.d, "causal": True,
-                                   "flops_per_step": fl},
+                                   "flops_per_step": fl} if do_p else None,
                        "decode": {"B": dc.B, "Hq": dc.Hq, "Hkv": dc.Hkv, "d": dc.d,
                                   "kv_len": [dc.len_lo, dc.len_hi], "splits": S,
-                                  "kv_bytes_per_step": kvb},
+                                  "kv_bytes_per_step": kvb} if do_d else None,
                        "l2": "inputs larger than L2 (no flush)",
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk_t, "unit": "TFLOP/s",
-                         "frac": achieved / pk_t, "traffic": traffic,
-                         "peak_kind": f"{peak_src} bf16 burst",
-                         "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                         "kernel": "prefill", "ms_per_launch": t_prefill},
-            "decode": {"metric": "KV GB/s (decode)", "value": dec_gbs * world, "unit": "GB/s",
-                       "path_value": dec_path_gbs * world,
-                       "ms_decode": t_decode, "ms_combine": t_combine,
-                       "roofline": {"bound": "hbm", "achieved": dec_gbs,
-                                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                    "frac": dec_gbs / peaks["hbm_gbs"], "traffic": dec_traffic,
-                                    "peak_kind": f"{peak_src} copy bandwidth"}},
-            "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": 3 * args.steps,
+            "roofline": roof,
+            "decode": decode_obj,
+            "e2e": e2e,
+            "gpu_launches": nl * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
+            "other_workloads": others,
         }
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -437,12 +553,18 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the secondary GQA sweep / long-decode measurements")
+    ap.add_argument("--kernel", choices=["all", "prefill", "decode"], default="all",
+                    help="time the whole step (default) or one form only (profiling)")
+    ap.add_argument("--small", action="store_true",
+                    help="decode on a quarter of the batch (profiling captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

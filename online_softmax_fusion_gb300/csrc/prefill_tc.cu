@@ -317,6 +317,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mx4[2] = max3(mx4[2], s[c + 4], s[c + 5]);
                     mx4[3] = max3(mx4[3], s[c + 6], s[c + 7]);
                 }
+            } else if (ALIBI && CAUSAL && !need_mask) {
+                // every key of this tile is at or before every row of the
+                // warp: bias = slope * (key - i'), built from an exact integer
+                // counter c and one packed FMA per key pair, then fused into
+                // the scale: x = s * scale + slope * c + slope * (k0 - i')
+                const float b0 = slope_l2 * float(k0 - i_al);
+                const uint64_t slope2 = f2_pack(slope_l2, slope_l2);
+                const uint64_t b02 = f2_pack(b0, b0);
+                const uint64_t sc2 = f2_pack(sl2, sl2);
+                const uint64_t two2 = f2_pack(2.f, 2.f);
+                uint64_t cc2 = f2_pack(0.f, 1.f);
+#pragma unroll
+                for (int c = 0; c < 128; c += 2) {
+                    const uint64_t bias2 = f2_fma(cc2, slope2, b02);
+                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sc2, bias2), s[c], s[c + 1]);
+                    mx4[(c >> 1) & 3] = max3(mx4[(c >> 1) & 3], s[c], s[c + 1]);
+                    cc2 = f2_add(cc2, two2);
+                }
             } else {
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
