@@ -100,3 +100,17 @@ def test_reference_arm_prints_contract_line(monkeypatch, capsys):
     assert line["impl"] == "reference"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert abs(line["value"] - 2e9 / 0.5 / 1e12) < 1e-12
+
+
+def test_clock_summary_keeps_only_samples_inside_the_region():
+    lines = [
+        "2026/12/02 07:00:00.000, 0, 2070, 2070, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 07:00:01.000, 0, 1500, 2070, 1300.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 07:00:01.100, 0, 1480, 2070, 1350.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 07:00:03.000, 0, 2070, 2070, 140.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    t0 = bench.ClockSampler._epoch("2026/12/02 07:00:00.900")
+    t1 = bench.ClockSampler._epoch("2026/12/02 07:00:01.200")
+    c = bench.ClockSampler.summarize(lines, t0, t1)
+    assert c["samples_in_region"] == 2 and c["sm_mhz"] == 1490.0
+    assert c["reasons"] == ["sw_power_cap"] and c["sm_max_mhz"] == 2070.0
