@@ -197,6 +197,13 @@ const char* attn_status_string(int status);
  * ATTN_ERR_CUDA when synchronisation itself failed. */
 int attn_device_status(void* stream);
 
+/* Self-test of the library's failure detection (no counterpart in the pages):
+ * launches a one-thread kernel that waits on a barrier nothing signals, with
+ * a time limit of limit_ms (1..10000), through the same bounded-wait code all
+ * kernels use. The kernel records ATTN_ERR_TIMEOUT in the device status word
+ * and returns; the context stays usable. Returns the launch status. */
+int attn_selftest_wait_timeout(int limit_ms, void* stream);
+
 /* Library ABI version (major * 100 + minor). */
 int attn_version(void);
 

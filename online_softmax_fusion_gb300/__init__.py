@@ -47,6 +47,7 @@ SIGNATURES = {
     "attn_status_string": (ctypes.c_char_p, [_c_int]),
     "attn_device_status": (_c_int, [_c_void_p]),
     "attn_version": (_c_int, []),
+    "attn_selftest_wait_timeout": (_c_int, [_c_int, _c_void_p]),
 }
 
 _lib = None
@@ -234,6 +235,12 @@ def decode_noalloc(q, k, v, kv_lens=None, scale=None, num_splits=0, out=None, ls
                                    d, float(scale), num_splits, _ptr(out), _ptr(lse), _stream())
     _check(st, "attn_decode_noalloc")
     return out, lse
+
+
+def selftest_wait_timeout(limit_ms: int = 100):
+    """Runs the bounded-wait self-test kernel on the current stream; the
+    device status word then reads ATTN_ERR_TIMEOUT (see device_status)."""
+    _check(lib().attn_selftest_wait_timeout(int(limit_ms), _stream()), "attn_selftest_wait_timeout")
 
 
 def device_status() -> int:

@@ -94,6 +94,19 @@ int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
 
 }  // namespace
 
+// One thread waits on a barrier that nothing arrives on, with a short limit:
+// the bounded-wait path of every kernel, run to its end on purpose.
+__global__ void wait_timeout_selftest_kernel(unsigned long long limit_ns, int* status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        mbar_wait_limit(&bar, 0, &abort_flag, status, limit_ns);
+    }
+}
+
 }  // namespace attn
 
 using namespace attn;
@@ -126,6 +139,15 @@ int attn_device_status(void* stream) {
         if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
     }
     return v;
+}
+
+int attn_selftest_wait_timeout(int limit_ms, void* stream) {
+    if (limit_ms <= 0 || limit_ms > 10000) return ATTN_ERR_VALUE;
+    int* st = status_ptr();
+    if (!st) return ATTN_ERR_CUDA;
+    wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        (unsigned long long)limit_ms * 1000000ull, st);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int attn_prefill_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq,

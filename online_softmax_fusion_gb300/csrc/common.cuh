@@ -69,21 +69,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete. Returns false (and
-// sets *abort) when the CTA was aborted or the time limit passed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* status) {
+// sets *abort) when the CTA was aborted or `limit_ns` of wall-clock time
+// passed, recording ATTN_ERR_TIMEOUT in the status word in the latter case.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity,
+                                                volatile int* abort, int* status,
+                                                unsigned long long limit_ns) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
         if (mbar_try_wait(a, parity)) return true;
         if (*abort) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             *abort = 1;
             record_status(status, ATTN_ERR_TIMEOUT);
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          int* status) {
+    return mbar_wait_limit(bar, parity, abort, status, kWaitLimitNs);
 }
 
 // ----------------------------------------------------------------------- TMA
