@@ -24,6 +24,12 @@ Readings where the pages are silent (each one is listed in the design notes):
   * ALiBi adds -slope_h * |i' - j| (i' the aligned row) after scaling; it is
     not multiplied by s;
   * GQA maps query head h to KV head floor(h / G), G = Hq / Hkv;
+  * SoftCap (named in §9, not defined there) replaces the scaled score x by
+    cap * tanh(x / cap) before the bias, the mask and the softmax;
+  * Window (named in §9, not defined there) is local attention: aligned row
+    i' sees keys j with i' - window_left <= j <= i' + window_right (a
+    negative bound means unlimited on that side); with causal, keys after i'
+    stay masked;
   * a row that sees no key has O = 0 and LSE = -inf;
   * a split of the Split-K form stores its normalised output O_s = O/l and
     its LSE_s = m + ln l; the merge recovers the raw sums from them.
@@ -51,7 +57,8 @@ def _f64(x) -> np.ndarray:
 
 
 def attend_head(q_rows, row_pos, k, v, *, scale, causal=False, slope=None,
-                Lq=None, Lk=None, kv_len=None):
+                Lq=None, Lk=None, kv_len=None, softcap=0.0, window_left=-1,
+                window_right=-1):
     """Attention of some query rows of one head against one K/V head.
 
     q_rows  [n, d]   query rows (any float dtype; upcast exactly to fp64)
@@ -59,6 +66,9 @@ def attend_head(q_rows, row_pos, k, v, *, scale, causal=False, slope=None,
     k, v    [Lk_buf, d]
     Lq, Lk  nominal lengths used for causal alignment (default: n rows / len(k))
     kv_len  keys [0, kv_len) are visible (default Lk)
+    softcap > 0: scores become softcap * tanh(score / softcap)
+    window_left / window_right >= 0: keys outside
+            [i' - window_left, i' + window_right] are not visible
 
     Returns (O [n, d] fp64, LSE [n] fp64).
     Follows Neptune论文浅读 §2: materialise the scores, take the row max, then
@@ -82,12 +92,18 @@ def attend_head(q_rows, row_pos, k, v, *, scale, causal=False, slope=None,
     kk = kk[:kv_len]
     vv = vv[:kv_len]
     x = scale * (q @ kk.T)                                  # [n, kv_len]
+    if softcap and softcap > 0.0:
+        x = float(softcap) * np.tanh(x / float(softcap))
     j = np.arange(kv_len, dtype=np.int64)[None, :]
     i_al = (pos + (Lk - Lq))[:, None]                       # bottom-right aligned row
     if slope is not None:
         x = x - float(slope) * np.abs(i_al - j).astype(np.float64)
     if causal:
         x = np.where(j > i_al, NEG_INF, x)
+    if window_left is not None and window_left >= 0:
+        x = np.where(j < i_al - int(window_left), NEG_INF, x)
+    if window_right is not None and window_right >= 0:
+        x = np.where(j > i_al + int(window_right), NEG_INF, x)
     m = x.max(axis=1)                                       # pass 1: row max
     live = np.isfinite(m)
     if not live.any():
@@ -103,7 +119,8 @@ def attend_head(q_rows, row_pos, k, v, *, scale, causal=False, slope=None,
 
 
 def attention_ref(q, k, v, *, scale, causal=False, alibi_slopes=None,
-                  rows=None, heads=None, batches=None, block_rows=512):
+                  rows=None, heads=None, batches=None, block_rows=512,
+                  softcap=0.0, window_left=-1, window_right=-1):
     """Batched attention with GQA, causal mask and ALiBi.
 
     q [B, Hq, Lq, d], k/v [B, Hkv, Lk, d] (numpy arrays or torch tensors).
@@ -133,7 +150,8 @@ def attention_ref(q, k, v, *, scale, causal=False, alibi_slopes=None,
                 qr = _f64(q[b, h][rr])
                 o, lse = attend_head(qr, rr, kh, vh, scale=scale, causal=causal,
                                      slope=None if slopes is None else slopes[h],
-                                     Lq=Lq, Lk=Lk)
+                                     Lq=Lq, Lk=Lk, softcap=softcap,
+                                     window_left=window_left, window_right=window_right)
                 O[bi, hi, r0:r0 + len(rr)] = o
                 L[bi, hi, r0:r0 + len(rr)] = lse
     return O, L

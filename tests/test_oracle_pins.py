@@ -352,3 +352,69 @@ def test_oracle_is_independent_of_product():
     src = inspect.getsource(oracle.attention)
     assert "online_softmax_fusion_gb300" not in src
     assert "ctypes" not in src
+
+
+# ------------------------------------------------ SoftCap and Window variants
+def test_softcap_matches_sdpa_with_capped_scores():
+    """SoftCap: scores become cap * tanh(score / cap). Library check: fp64 SDPA
+    fed the capped logits through an additive mask on zero queries."""
+    Lq, Lk, d, s, cap = 12, 20, 8, 0.9, 2.5
+    q = _rand(Lq, d) * 3
+    k = _rand(Lk, d) * 3
+    v = _rand(Lk, d)
+    o, lse = attend_head(q, np.arange(Lq), k, v, scale=s, softcap=cap, Lq=Lq, Lk=Lk)
+    capped = cap * np.tanh(s * (q @ k.T) / cap)
+    ref = _sdpa(np.zeros((1, 1, Lq, d)), k[None, None], v[None, None], capped[None, None], 1.0)[0, 0]
+    assert np.max(np.abs(o - ref)) < 1e-12
+    assert np.max(np.abs(lse - _lse_torch(np.zeros((1, 1, Lq, d)), k[None, None], capped[None, None], 1.0)[0, 0])) < 1e-12
+    # bounded logits: |x| < cap, so LSE <= cap + ln(Lk)
+    assert np.all(lse < cap + math.log(Lk))
+    # a cap far above the logits changes nothing (tanh(z) ~ z)
+    o2, l2 = attend_head(q, np.arange(Lq), k, v, scale=s, softcap=1e7, Lq=Lq, Lk=Lk)
+    o3, l3 = attend_head(q, np.arange(Lq), k, v, scale=s, Lq=Lq, Lk=Lk)
+    assert np.max(np.abs(o2 - o3)) < 1e-9 and np.max(np.abs(l2 - l3)) < 1e-9
+
+
+def test_window_zero_selects_the_aligned_key():
+    """Window 0 on both sides: row i' sees only key i', so O_i = v_{i'} and
+    LSE = its scaled score."""
+    Lq, Lk, d = 9, 14, 6
+    q = _rand(Lq, d)
+    k = _rand(Lk, d)
+    v = _rand(Lk, d)
+    o, lse = attend_head(q, np.arange(Lq), k, v, scale=0.7, window_left=0, window_right=0,
+                         Lq=Lq, Lk=Lk)
+    for i in range(Lq):
+        ia = i + Lk - Lq
+        assert np.max(np.abs(o[i] - v[ia])) < 1e-15
+        assert abs(lse[i] - 0.7 * float(q[i] @ k[ia])) < 1e-13
+
+
+def test_window_uniform_closed_form():
+    """Q = 0, causal, left window w: row i' averages keys max(0, i'-w)..i'; with
+    v_j = j, O = (lo + i') / 2 and LSE = ln(i' - lo + 1)."""
+    L, w = 30, 7
+    q = np.zeros((L, 3))
+    k = _rand(L, 3)
+    v = np.tile(np.arange(L, dtype=np.float64)[:, None], (1, 3))
+    o, lse = attend_head(q, np.arange(L), k, v, scale=1.0, causal=True, window_left=w)
+    for i in range(L):
+        lo = max(0, i - w)
+        assert abs(o[i, 0] - (lo + i) / 2.0) < 1e-12
+        assert abs(lse[i] - math.log(i - lo + 1)) < 1e-12
+
+
+def test_window_matches_sdpa_with_band_mask():
+    Lq = Lk = 25
+    q = _rand(1, 2, Lq, 8)
+    k = _rand(1, 2, Lk, 8)
+    v = _rand(1, 2, Lk, 8)
+    wl, wr = 4, 2
+    mask = np.full((1, 2, Lq, Lk), -math.inf)
+    for i in range(Lq):
+        for j in range(Lk):
+            if i - wl <= j <= i + wr:
+                mask[:, :, i, j] = 0.0
+    O, L = attention_ref(q, k, v, scale=0.5, window_left=wl, window_right=wr)
+    assert np.max(np.abs(O - _sdpa(q, k, v, mask, 0.5))) < 1e-12
+    assert np.max(np.abs(L - _lse_torch(q, k, mask, 0.5))) < 1e-12
