@@ -97,6 +97,34 @@ int attn_prefill_ex(const void* Q, const void* K, const void* V,
                     int impl, void* stream);
 
 /*
+ * Options of attn_prefill_opts: the attention variants Neptune论文浅读 §9
+ * evaluates (Global, Causal, ALiBi, GQA, SoftCap, Window). The page names
+ * SoftCap and Window without defining them; this library reads them as:
+ *   softcap > 0  the scaled score x becomes softcap * tanh(x / softcap)
+ *                (before the ALiBi bias and the masks); 0 = off;
+ *   window_left  >= 0: query row i sees no key j < i' - window_left;
+ *   window_right >= 0: query row i sees no key j > i' + window_right;
+ *                < 0 = unlimited; i' = i + (Lk - Lq) as for the causal mask.
+ * KV tiles wholly outside a window are skipped, not just masked.
+ */
+typedef struct {
+    int causal;                  /* as attn_prefill                          */
+    float scale;                 /* softmax scale (finite)                   */
+    const float* alibi_slopes;   /* NULL or device fp32 [Hq]                 */
+    float softcap;               /* >= 0, finite; 0 = off                    */
+    int window_left;             /* < 0 = unlimited                          */
+    int window_right;            /* < 0 = unlimited                          */
+    int impl;                    /* ATTN_IMPL_*; softcap / window need the
+                                    tcgen05 kernel (mma.sync: UNSUPPORTED)  */
+} attn_prefill_options;
+
+/* attn_prefill with the variants above (same tensors and layouts). */
+int attn_prefill_opts(const void* Q, const void* K, const void* V,
+                      void* O, float* LSE,
+                      int B, int Hq, int Hkv, int Lq, int Lk, int d,
+                      const attn_prefill_options* opts, void* stream);
+
+/*
  * Split-K decode (Neptune论文浅读 §6; the split-KV decode of CMU 15-779
  * 第 11 讲 §7.1, which parallelises over batch x KV head x KV sequence and
  * stacks the G = Hq / Hkv query heads of a group as rows so that each K/V row

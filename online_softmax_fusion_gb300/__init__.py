@@ -29,11 +29,21 @@ _c_void_p = ctypes.c_void_p
 _c_int = ctypes.c_int
 _c_float = ctypes.c_float
 
+class PrefillOptions(ctypes.Structure):
+    """Mirror of attn_prefill_options (include/attn.h)."""
+    _fields_ = [("causal", ctypes.c_int), ("scale", ctypes.c_float),
+                ("alibi_slopes", ctypes.c_void_p), ("softcap", ctypes.c_float),
+                ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+                ("impl", ctypes.c_int)]
+
+
 # name -> (restype, argtypes); the full exported surface of include/attn.h
 SIGNATURES = {
     "attn_prefill": (_c_int, [_c_void_p] * 5 + [_c_int] * 7 + [_c_float, _c_void_p, _c_void_p]),
     "attn_prefill_ex": (_c_int, [_c_void_p] * 5 + [_c_int] * 7 + [_c_float, _c_void_p, _c_int,
                                                                    _c_void_p]),
+    "attn_prefill_opts": (_c_int, [_c_void_p] * 5 + [_c_int] * 6 + [ctypes.POINTER(PrefillOptions),
+                                                                     _c_void_p]),
     "attn_decode_num_splits": (_c_int, [_c_int] * 5),
     "attn_decode_split_len": (_c_int, [_c_int] * 2),
     "attn_decode_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
@@ -51,6 +61,7 @@ SIGNATURES = {
 }
 
 _lib = None
+
 
 
 class AttnError(RuntimeError):
@@ -104,8 +115,10 @@ def _req(t, name, dtype, dims):
 
 
 def prefill(q, k, v, causal=False, scale=None, alibi_slopes=None, impl="auto", out=None,
-            lse=None, with_lse=True):
+            lse=None, with_lse=True, softcap=0.0, window=(-1, -1)):
     """Fused attention forward. q [B,Hq,Lq,d], k/v [B,Hkv,Lk,d] bf16 CUDA.
+    softcap > 0 caps the scaled scores (cap * tanh(x / cap)); window =
+    (left, right) limits row i to keys [i' - left, i' + right] (-1 = no limit).
     Returns (O bf16 [B,Hq,Lq,d], LSE fp32 [B,Hq,Lq] or None)."""
     _req(q, "q", torch.bfloat16, 4)
     _req(k, "k", torch.bfloat16, 4)
@@ -122,9 +135,16 @@ def prefill(q, k, v, causal=False, scale=None, alibi_slopes=None, impl="auto", o
         out = torch.empty_like(q)
     if lse is None and with_lse:
         lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
-    st = lib().attn_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Lq,
-                               Lk, d, int(bool(causal)), float(scale), _ptr(alibi_slopes),
-                               IMPLS[impl], _stream())
+    if softcap or tuple(window) != (-1, -1):
+        opts = PrefillOptions(int(bool(causal)), float(scale),
+                              None if alibi_slopes is None else alibi_slopes.data_ptr(),
+                              float(softcap), int(window[0]), int(window[1]), IMPLS[impl])
+        st = lib().attn_prefill_opts(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv,
+                                     Lq, Lk, d, ctypes.byref(opts), _stream())
+    else:
+        st = lib().attn_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv,
+                                   Lq, Lk, d, int(bool(causal)), float(scale), _ptr(alibi_slopes),
+                                   IMPLS[impl], _stream())
     _check(st, "attn_prefill")
     return out, lse
 

@@ -150,9 +150,14 @@ int attn_selftest_wait_timeout(int limit_ms, void* stream) {
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_prefill_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq,
-                    int Hkv, int Lq, int Lk, int d, int causal, float scale,
-                    const float* alibi_slopes, int impl, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int prefill_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq,
+                 int Hkv, int Lq, int Lk, int d, int causal, float scale,
+                 const float* alibi_slopes, float softcap, int window_left, int window_right,
+                 int impl, void* stream) {
     if (!Q || !K || !V || !O) return ATTN_ERR_NULL;
     int st = check_common(B, Hq, Hkv, d, scale);
     if (st) return st;
@@ -162,6 +167,8 @@ int attn_prefill_ex(const void* Q, const void* K, const void* V, void* O, float*
         (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)))
         return ATTN_ERR_ALIGN;
     if (impl < ATTN_IMPL_AUTO || impl > ATTN_IMPL_MMA_SYNC) return ATTN_ERR_UNSUPPORTED;
+    if (!std::isfinite(softcap) || softcap < 0.f) return ATTN_ERR_VALUE;
+    const bool extra = softcap > 0.f || window_left >= 0 || window_right >= 0;
 
     PrefillLaunch L;
     std::memset(&L, 0, sizeof(L));
@@ -176,6 +183,9 @@ int attn_prefill_ex(const void* Q, const void* K, const void* V, void* O, float*
     L.p.G = Hq / Hkv;
     L.p.scale_log2 = scale * kLog2e;
     L.p.causal = causal ? 1 : 0;
+    L.p.softcap = softcap;
+    L.p.window_left = window_left < 0 ? -1 : window_left;
+    L.p.window_right = window_right < 0 ? -1 : window_right;
     L.p.pair_heads = (L.p.G % 2 == 0) ? 1 : 0;
     L.p.status = status_ptr();
     if (!L.p.status) return ATTN_ERR_CUDA;
@@ -189,10 +199,32 @@ int attn_prefill_ex(const void* Q, const void* K, const void* V, void* O, float*
         st = launch_prefill_tc(L, d, s);
         if (st != ATTN_ERR_UNSUPPORTED || impl == ATTN_IMPL_TCGEN05) return st;
     }
+    // the register-tile kernel has no softcap / window variants
+    if (extra) return ATTN_ERR_UNSUPPORTED;
     if ((st = make_map(&L.tmQ, Q, d, Lq, (long long)B * Hq, kMmaBM))) return st;
     if ((st = make_map(&L.tmK, K, d, Lk, (long long)B * Hkv, kMmaBN))) return st;
     if ((st = make_map(&L.tmV, V, d, Lk, (long long)B * Hkv, kMmaBN))) return st;
     return launch_prefill_mma(L, d, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_prefill_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq,
+                    int Hkv, int Lq, int Lk, int d, int causal, float scale,
+                    const float* alibi_slopes, int impl, void* stream) {
+    return prefill_impl(Q, K, V, O, LSE, B, Hq, Hkv, Lq, Lk, d, causal, scale, alibi_slopes, 0.f,
+                        -1, -1, impl, stream);
+}
+
+int attn_prefill_opts(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                      int Hq, int Hkv, int Lq, int Lk, int d, const attn_prefill_options* opts,
+                      void* stream) {
+    if (!opts) return ATTN_ERR_NULL;
+    return prefill_impl(Q, K, V, O, LSE, B, Hq, Hkv, Lq, Lk, d, opts->causal, opts->scale,
+                        opts->alibi_slopes, opts->softcap, opts->window_left, opts->window_right,
+                        opts->impl, stream);
 }
 
 int attn_prefill(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq,

@@ -37,6 +37,9 @@ struct PrefillParams {
     int B, Hq, Hkv, Lq, Lk, G;
     float scale_log2;         // softmax scale * log2(e)
     int causal;
+    float softcap;            // > 0: scores -> softcap * tanh(score / softcap)
+    int window_left;          // >= 0: keys before i' - window_left are masked
+    int window_right;         // >= 0: keys after i' + window_right are masked
     int pair_heads;           // tcgen05 kernel: a CTA's two Q tiles are two query
                               // heads of one KV group (1) or two row blocks (0)
     int* status;

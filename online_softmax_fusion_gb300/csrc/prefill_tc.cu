@@ -66,25 +66,32 @@ struct TcSmem {
     int abort;
 };
 
-struct TileInfo {
-    int head;    // query head
-    int row0;    // first query row
-    int n;       // KV tiles this Q tile needs
+// KV tiles [lo, hi) that the 128 query rows starting at row0 can see.
+struct KvRange {
+    int lo, hi;
 };
 
-__device__ __forceinline__ int kv_tiles_for(int row0, int Lq, int Lk, int causal) {
-    if (row0 >= Lq) return 0;
-    int kend = Lk;
-    if (causal) {
-        const int last = min(row0 + 127, Lq - 1);
-        kend = min(Lk, last + (Lk - Lq) + 1);
-    }
-    return kend > 0 ? (kend + 127) / 128 : 0;
+__device__ __forceinline__ KvRange kv_range_for(int row0, const PrefillParams& p, bool causal) {
+    KvRange r{0, 0};
+    if (row0 >= p.Lq) return r;
+    const int off = p.Lk - p.Lq;
+    const int last = min(row0 + 127, p.Lq - 1);
+    int kend = p.Lk;
+    if (causal) kend = min(kend, last + off + 1);
+    if (p.window_right >= 0) kend = min(kend, last + off + p.window_right + 1);
+    int kbeg = 0;
+    if (p.window_left >= 0) kbeg = max(0, row0 + off - p.window_left);
+    if (kend <= kbeg) return r;
+    r.lo = kbeg / 128;
+    r.hi = (kend + 127) / 128;
+    return r;
 }
 
 }  // namespace
 
-template <int D, bool CAUSAL, bool ALIBI>
+// EXTRA: softcap and/or a sliding window is set (all tiles take the
+// per-element path).
+template <int D, bool CAUSAL, bool ALIBI, bool EXTRA>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
@@ -111,10 +118,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int head1 = pair_heads ? 2 * hb + 1 : hb;
     const int row00 = pair_heads ? rb * 128 : rb * 256;
     const int row01 = pair_heads ? rb * 128 : rb * 256 + 128;
-    const int n0 = kv_tiles_for(row00, p.Lq, p.Lk, CAUSAL);
-    const int n1 = kv_tiles_for(row01, p.Lq, p.Lk, CAUSAL);
+    const KvRange rg0 = kv_range_for(row00, p, CAUSAL);
+    const KvRange rg1 = kv_range_for(row01, p, CAUSAL);
     const int kvh = head0 / p.G;
-    const int n = max(n0, n1);
+    // the CTA streams the union of its tiles' KV ranges
+    const bool e0 = rg0.hi <= rg0.lo, e1 = rg1.hi <= rg1.lo;
+    const int jlo = e0 ? rg1.lo : (e1 ? rg0.lo : min(rg0.lo, rg1.lo));
+    const int jhi = e0 ? rg1.hi : (e1 ? rg0.hi : max(rg0.hi, rg1.hi));
+    const int n = (e0 && e1) ? 0 : jhi - jlo;
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.bar_q, 1);
@@ -167,7 +178,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const CUtensorMap* map = (u & 1) ? &tmV : &tmK;
 #pragma unroll
                 for (int bx = 0; bx < Cfg::kBoxes; ++bx)
-                    tma_load_3d(sm.kv[slot][bx], map, &sm.kv_full[slot], bx * 64, (u >> 1) * 128, z);
+                    tma_load_3d(sm.kv[slot][bx], map, &sm.kv_full[slot], bx * 64,
+                                (jlo + (u >> 1)) * 128, z);
                 issued = u + 1;
             }
         }
@@ -177,7 +189,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         {
             constexpr uint32_t idS = tc::idesc_bf16(128, 128, 0);
             constexpr uint32_t idO = tc::idesc_bf16(128, D, 1);
-            const int nt[2] = {n0, n1};
             bool ok = mbar_wait(&sm.bar_q, 0, abort, p.status);
             tc::fence_after_sync();
             int u = 0;   // next ring entry to consume
@@ -209,58 +220,67 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc::mma_bf16_ss_warp(d, a0 + o, b0 + o, idS, kk > 0);
                 }
             };
-            auto issue_pv = [&](int t, int slot, int j) {
+            auto issue_pv = [&](int t, int slot, bool first) {
                 const uint64_t b0 = vdesc0 + uint64_t(uint32_t(slot) * kSlotStep);
                 const uint32_t tP = tbase + t * 128 + 64;
                 const uint32_t d = tbase + 256 + t * D;
-                const uint32_t acc0 = j > 0 ? 1u : 0u;
+                const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     tc::mma_bf16_ts_warp(d, tP + kk * 8, b0 + uint32_t(kk * (2048 >> 4)), idO,
                                     kk > 0 ? 1u : acc0);
             };
+            const KvRange rg[2] = {rg0, rg1};
+            int pf[2] = {0, 0};   // softmax steps consumed per tile (p_full phases)
             if (ok && n > 0) {
-                const int ks = acquire();
+                const int ks = acquire();           // K_jlo
                 ok = ks >= 0;
                 if (ok) {
                     for (int t = 0; t < 2; ++t)
-                        if (nt[t] > 0) {
+                        if (rg[t].lo == jlo && rg[t].hi > rg[t].lo) {
                             issue_s(t, ks);
                             tc::commit_warp(&sm.s_full[t]);
                         }
                     release(ks);
                 }
             }
-            for (int j = 0; ok && j < n; ++j) {
+            for (int jj = 0; ok && jj < n; ++jj) {
+                const int j = jlo + jj;
                 const int vs = acquire();           // V_j
                 if (vs < 0) break;
                 int ks = -1;
+                auto get_k = [&]() {                // K_{j+1} follows V_j in the ring
+                    if (ks < 0) {
+                        ++u;
+                        ks = acquire();
+                        --u;
+                    }
+                    return ks >= 0;
+                };
                 for (int t = 0; ok && t < 2; ++t) {
-                    if (j >= nt[t]) continue;
-                    ok = mbar_wait(&sm.p_full[t], j & 1, abort, p.status);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    issue_pv(t, vs, j);
-                    if (j + 1 < nt[t]) {
-                        if (ks < 0) {
-                            ++u;                    // K_{j+1} follows V_j in the ring
-                            ks = acquire();
-                            --u;
-                            if (ks < 0) { ok = false; break; }
-                        }
+                    const bool active = j >= rg[t].lo && j < rg[t].hi;
+                    if (active) {
+                        ok = mbar_wait(&sm.p_full[t], pf[t] & 1, abort, p.status);
+                        if (!ok) break;
+                        ++pf[t];
+                        tc::fence_after_sync();
+                        issue_pv(t, vs, j == rg[t].lo);
+                    }
+                    const bool next_s = (active && j + 1 < rg[t].hi) ||
+                                        (j + 1 == rg[t].lo && rg[t].hi > rg[t].lo);
+                    if (next_s) {
+                        if (!get_k()) { ok = false; break; }
                         issue_s(t, ks);
                         tc::commit_warp(&sm.s_full[t]);
-                    } else {
+                    } else if (active) {
                         tc::commit_warp(&sm.o_done[t]);
                     }
                 }
                 if (!ok) break;
                 release(vs);
-                if (j + 1 < n) {
-                    // every tile that needs K_{j+1} has consumed it by now; a
-                    // tile that does not (the shorter causal tile) never waits
-                    if (ks < 0) ks = acquire();
-                    if (ks < 0) break;
+                if (jj + 1 < n) {
+                    // every tile that needs K_{j+1} has consumed it by now
+                    if (!get_k()) break;
                     release(ks);
                 }
             }
@@ -278,7 +298,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int r = q4 * 32 + lane;             // row within the tile
         const int head = t ? head1 : head0;
         const int row0 = t ? row01 : row00;
-        const int ntile = t ? n1 : n0;
+        const KvRange rgt = t ? rg1 : rg0;
+        const int ntile = rgt.hi > rgt.lo ? rgt.hi - rgt.lo : 0;
         const int row = row0 + r;
         const int i_al = row + off;               // bottom-right aligned row index
         const uint32_t lane_off = uint32_t(q4 * 32) << 16;
@@ -286,13 +307,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t tP = tS + 64;
         const uint32_t tO = tbase + 256 + t * D + lane_off;
         const float sl2 = p.scale_log2;
+        // softcap in the natural-log domain: score / cap, then * cap * log2(e)
+        const float sc_div = EXTRA && p.softcap > 0.f ? (sl2 / kLog2e) / p.softcap : 0.f;
+        const float cap_l2 = EXTRA && p.softcap > 0.f ? p.softcap * kLog2e : 0.f;
         const float slope_l2 = ALIBI ? p.slopes[head] * kLog2e : 0.f;
 
         float m = -INFINITY;   // reference max (log2 domain)
         float l = 0.f;
         bool ok = true;
-        for (int j = 0; j < ntile; ++j) {
-            ok = mbar_wait(&sm.s_full[t], j & 1, abort, p.status);
+        for (int jt = 0; jt < ntile; ++jt) {
+            const int j = rgt.lo + jt;
+            ok = mbar_wait(&sm.s_full[t], jt & 1, abort, p.status);
             if (!ok) break;
             tc::fence_after_sync();
             float s[128];
@@ -303,8 +328,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(rr[i]);
             }
             const int k0 = j * 128;
-            const bool need_mask =
-                (k0 + 128 > p.Lk) || (CAUSAL && k0 + 127 > row0 + q4 * 32 + off);
+            const bool need_mask = EXTRA || (k0 + 128 > p.Lk) ||
+                                   (CAUSAL && k0 + 127 > row0 + q4 * 32 + off);
             // x = s * scale (log2 domain) + bias, masked; on unmasked tiles
             // without bias the scale is folded into the exp's FMA below
             const bool fast = !need_mask && !ALIBI && sl2 > 0.f;
@@ -339,12 +364,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
                     const int key = k0 + c;
-                    float x = s[c] * sl2;
+                    float x;
+                    if (EXTRA && p.softcap > 0.f) {
+                        // cap * tanh(score / cap), tanh(y) = (e - 1) / (e + 1)
+                        // with e = 2^(2 y log2 e); |y| <= 15 keeps e finite
+                        // and tanh(15) rounds to 1 in fp32
+                        const float y = fminf(fmaxf(s[c] * sc_div, -15.f), 15.f);
+                        const float e = ex2(y * (2.f * kLog2e));
+                        x = cap_l2 * ((e - 1.f) * rcp_approx(e + 1.f));
+                    } else {
+                        x = s[c] * sl2;
+                    }
                     if (ALIBI) {
                         const float dist = float(i_al - key);
                         x -= slope_l2 * (CAUSAL ? dist : fabsf(dist));
                     }
-                    if (need_mask && (key >= p.Lk || (CAUSAL && key > i_al))) x = -INFINITY;
+                    bool masked = key >= p.Lk || (CAUSAL && key > i_al);
+                    if (EXTRA) {
+                        masked = masked || (p.window_left >= 0 && key < i_al - p.window_left) ||
+                                 (p.window_right >= 0 && key > i_al + p.window_right);
+                    }
+                    if (masked) x = -INFINITY;
                     s[c] = x;
                     mx4[c & 3] = fmaxf(mx4[c & 3], x);
                 }
@@ -355,7 +395,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // exceeds it by more than the threshold (or it is still unset)
             float m_new = m;
             if (mx > m + kRescaleThreshold || (m == -INFINITY && mx != -INFINITY)) m_new = mx;
-            const bool rescale = (j > 0) && (m != -INFINITY) && (m_new != m);
+            const bool rescale = (jt > 0) && (m != -INFINITY) && (m_new != m);
             const float corr = rescale ? ex2(m - m_new) : 1.f;
             const float m_use = m_new == -INFINITY ? 0.f : m_new;
             // p = 2^(x - m) as one packed FMA per key pair (x = s * scale on
@@ -467,14 +507,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 namespace {
 
-template <int D, bool CAUSAL, bool ALIBI>
+template <int D, bool CAUSAL, bool ALIBI, bool EXTRA>
 int launch_tc_t(const PrefillLaunch& L, cudaStream_t stream) {
     const size_t smem = sizeof(TcSmem<D>) + 1024;
     static bool attr_set[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(prefill_tc_kernel<D, CAUSAL, ALIBI>,
+        if (cudaFuncSetAttribute(prefill_tc_kernel<D, CAUSAL, ALIBI, EXTRA>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(smem)) != cudaSuccess)
             return ATTN_ERR_CUDA;
@@ -485,17 +525,25 @@ int launch_tc_t(const PrefillLaunch& L, cudaStream_t stream) {
     const long long items = (long long)((L.p.Lq + rows_per_item - 1) / rows_per_item) * n_hb;
     if (items > 0x7fffffffLL) return ATTN_ERR_SHAPE;
     dim3 grid(unsigned(items), L.p.B);
-    prefill_tc_kernel<D, CAUSAL, ALIBI><<<grid, kTcThreads, smem, stream>>>(L.tmQ, L.tmK, L.tmV,
+    prefill_tc_kernel<D, CAUSAL, ALIBI, EXTRA><<<grid, kTcThreads, smem, stream>>>(L.tmQ, L.tmK, L.tmV,
                                                                            L.p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-template <int D>
-int launch_tc_d(const PrefillLaunch& L, cudaStream_t stream) {
+template <int D, bool EXTRA>
+int launch_tc_e(const PrefillLaunch& L, cudaStream_t stream) {
     const bool alibi = L.p.slopes != nullptr;
     if (L.p.causal)
-        return alibi ? launch_tc_t<D, true, true>(L, stream) : launch_tc_t<D, true, false>(L, stream);
-    return alibi ? launch_tc_t<D, false, true>(L, stream) : launch_tc_t<D, false, false>(L, stream);
+        return alibi ? launch_tc_t<D, true, true, EXTRA>(L, stream)
+                     : launch_tc_t<D, true, false, EXTRA>(L, stream);
+    return alibi ? launch_tc_t<D, false, true, EXTRA>(L, stream)
+                 : launch_tc_t<D, false, false, EXTRA>(L, stream);
+}
+
+template <int D>
+int launch_tc_d(const PrefillLaunch& L, cudaStream_t stream) {
+    const bool extra = L.p.softcap > 0.f || L.p.window_left >= 0 || L.p.window_right >= 0;
+    return extra ? launch_tc_e<D, true>(L, stream) : launch_tc_e<D, false>(L, stream);
 }
 
 }  // namespace

@@ -148,3 +148,56 @@ def test_impls_agree_closely(attn):
     Ob, Lb = attn.prefill(q, k, v, causal=True, impl="mma_sync")
     assert (Oa.float() - Ob.float()).abs().max().item() < 2e-2
     assert (La - Lb).abs().max().item() < 1e-4
+
+
+# ------------------------------------------------------ SoftCap and Window
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,d,causal,alibi,softcap,window", [
+    (1, 2, 2, 300, 300, 128, True, False, 20.0, (-1, -1)),     # softcap, causal, ragged
+    (1, 4, 2, 256, 256, 128, False, False, 5.0, (-1, -1)),     # tight cap, non-causal
+    (1, 2, 2, 700, 700, 128, True, False, 0.0, (200, -1)),     # sliding window, causal
+    (2, 4, 2, 513, 513, 64, False, False, 0.0, (64, 100)),     # two-sided window, d = 64
+    (1, 8, 2, 640, 640, 128, True, True, 30.0, (300, -1)),     # softcap + window + ALiBi + GQA
+    (1, 2, 2, 100, 400, 128, True, False, 0.0, (50, -1)),      # Lq < Lk with window
+    (1, 2, 2, 384, 384, 128, True, False, 0.0, (0, -1)),       # window 0: the diagonal only
+])
+def test_prefill_softcap_window(attn, B, Hq, Hkv, Lq, Lk, d, causal, alibi, softcap, window):
+    q = _rand((B, Hq, Lq, d), Lq + 1, 2.0)
+    k = _rand((B, Hkv, Lk, d), Lk + 2, 2.0)
+    v = _rand((B, Hkv, Lk, d), Lk + 3)
+    slopes = W.alibi_slopes(Hq) if alibi else None
+    scale = d ** -0.5
+    O, L = attn.prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale,
+                        alibi_slopes=None if slopes is None else slopes.cuda(),
+                        softcap=softcap, window=window)
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    Or, Lr = attention_ref(q, k, v, scale=scale, causal=causal, alibi_slopes=slopes,
+                           softcap=softcap, window_left=window[0], window_right=window[1])
+    assert_o_close(O, Or)
+    assert_lse_close(L, Lr)
+
+
+def test_window_long_sequence_sampled(attn):
+    """Causal sliding window of 1024 keys over L = 16384 (tiles outside the
+    window are skipped): sampled rows against the oracle."""
+    L, d, w = 16384, 128, 1024
+    q = _rand((1, 4, L, d), 1, 1.0).cuda()
+    k = _rand((1, 2, L, d), 2, 1.0).cuda()
+    v = _rand((1, 2, L, d), 3, 1.0).cuda()
+    O, Ls = attn.prefill(q, k, v, causal=True, window=(w, -1))
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    rows = W.sample_rows(L, 256, 64, 5).numpy()
+    for h in (0, 3):
+        Or, Lr = attention_ref(q[:, h:h + 1].cpu(), k[:, h // 2:h // 2 + 1].cpu(),
+                               v[:, h // 2:h // 2 + 1].cpu(), scale=d ** -0.5, causal=True,
+                               rows=rows, window_left=w)
+        idx = torch.from_numpy(rows).cuda()
+        assert_o_close(O[0, h].index_select(0, idx), Or[0, 0])
+        assert_lse_close(Ls[0, h].index_select(0, idx), Lr[0, 0])
+
+
+def test_softcap_window_unsupported_on_register_tile_kernel(attn):
+    q = torch.zeros(1, 1, 128, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(attn.AttnError):
+        attn.prefill(q, q, q, impl="mma_sync", softcap=10.0)
