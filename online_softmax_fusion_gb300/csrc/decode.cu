@@ -216,6 +216,9 @@ __global__ void __launch_bounds__(kDecThreads)
         }
     }
     __syncthreads();
+    // the combine grid may start launching now; it waits for this grid's
+    // completion (griddepcontrol.wait) before reading any partial
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (*abort) {
         // Let every copy this CTA issued land before the CTA's shared memory
@@ -278,6 +281,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
                                                       float* __restrict__ LSE) {
     extern __shared__ float wts[];   // [S]
     __shared__ float red[4];
+    // launched as a programmatic dependent of the decode: wait until that
+    // grid has completed and its partials are visible (no-op otherwise)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t bh = blockIdx.x;
     const float* lp = LSE_part + bh * S;
     const int tid = threadIdx.x;
@@ -341,16 +347,27 @@ int launch_combine(const float* O_part, const float* LSE_part, int B, int Hq, in
                    void* O, float* LSE, cudaStream_t stream) {
     const size_t smem = size_t(S) * sizeof(float);
     if (smem > 48 * 1024) return ATTN_ERR_WORKSPACE;
-    dim3 grid(unsigned(B) * unsigned(Hq));
+    // programmatic stream serialisation: the combine's launch may overlap the
+    // tail of a preceding decode grid (which signals launch_dependents)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(B) * unsigned(Hq));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    __nv_bfloat16* Ob = static_cast<__nv_bfloat16*>(O);
+    cudaError_t e;
     if (d == 64)
-        combine_kernel<64><<<grid, 128, smem, stream>>>(O_part, LSE_part, S,
-                                                        static_cast<__nv_bfloat16*>(O), LSE);
+        e = cudaLaunchKernelEx(&cfg, combine_kernel<64>, O_part, LSE_part, S, Ob, LSE);
     else if (d == 128)
-        combine_kernel<128><<<grid, 128, smem, stream>>>(O_part, LSE_part, S,
-                                                         static_cast<__nv_bfloat16*>(O), LSE);
+        e = cudaLaunchKernelEx(&cfg, combine_kernel<128>, O_part, LSE_part, S, Ob, LSE);
     else
         return ATTN_ERR_UNSUPPORTED;
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace attn
