@@ -11,6 +11,7 @@ special case and brute force on tiny inputs). Every public function is pinned.
 from .attention import (  # noqa: F401
     attend_head,
     attention_ref,
+    attention_backward_ref,
     decode_ref,
     decode_split_partials_ref,
     combine_ref,

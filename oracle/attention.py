@@ -284,3 +284,50 @@ def naive_fused_exp_sum(x):
         xmax = max(xmax, xj)
         s += math.exp(xj - xmax)
     return xmax, s
+
+
+def attention_backward_ref(q, k, v, dO, *, scale, causal=False, alibi_slopes=None):
+    """Gradients of attention (the backward pass; its single-pass structure on
+    tensor cores is described in the Twill review (xllm-io) §七 7.2).
+
+    Plain definition per (b, h), kv = h // G, with P the forward probabilities
+    (materialised, two-pass) and O = P V:
+      dV_j  = sum_i P_ij dO_i                  (summed over the group's heads)
+      dP_ij = dO_i . v_j
+      D_i   = sum_j P_ij dP_ij  (= dO_i . O_i)
+      dS_ij = P_ij (dP_ij - D_i)
+      dQ_i  = s sum_j dS_ij k_j
+      dK_j  = s sum_i dS_ij q_i                (summed over the group's heads)
+    Masked pairs have P = 0; the ALiBi bias does not depend on Q or K.
+    Returns (dQ [B,Hq,Lq,d], dK [B,Hkv,Lk,d], dV [B,Hkv,Lk,d]) in fp64.
+    """
+    qq, kk, vv, gg = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, Hq, Lq, d = qq.shape
+    Hkv, Lk = kk.shape[1], kk.shape[2]
+    G = Hq // Hkv
+    slopes = None if alibi_slopes is None else _f64(alibi_slopes).reshape(-1)
+    dQ = np.zeros_like(qq)
+    dK = np.zeros_like(kk)
+    dV = np.zeros_like(vv)
+    i_al = (np.arange(Lq) + (Lk - Lq))[:, None]
+    j = np.arange(Lk)[None, :]
+    for b in range(B):
+        for h in range(Hq):
+            kv = h // G
+            x = scale * (qq[b, h] @ kk[b, kv].T)
+            if slopes is not None:
+                x = x - slopes[h] * np.abs(i_al - j).astype(np.float64)
+            if causal:
+                x = np.where(j > i_al, NEG_INF, x)
+            m = x.max(axis=1, keepdims=True)
+            live = np.isfinite(m[:, 0])
+            P = np.zeros_like(x)
+            e = np.exp(x[live] - m[live])
+            P[live] = e / e.sum(axis=1, keepdims=True)
+            dV[b, kv] += P.T @ gg[b, h]
+            dP = gg[b, h] @ vv[b, kv].T
+            D = (P * dP).sum(axis=1, keepdims=True)
+            dS = P * (dP - D)
+            dQ[b, h] = scale * (dS @ kk[b, kv])
+            dK[b, kv] += scale * (dS.T @ qq[b, h])
+    return dQ, dK, dV

@@ -418,3 +418,85 @@ def test_window_matches_sdpa_with_band_mask():
     O, L = attention_ref(q, k, v, scale=0.5, window_left=wl, window_right=wr)
     assert np.max(np.abs(O - _sdpa(q, k, v, mask, 0.5))) < 1e-12
     assert np.max(np.abs(L - _lse_torch(q, k, mask, 0.5))) < 1e-12
+
+
+# ------------------------------------------------------------- backward pass
+@pytest.mark.parametrize("Lq,Lk,causal,G,alibi", [
+    (12, 12, False, 1, False),
+    (17, 17, True, 2, False),
+    (9, 21, True, 1, True),      # Lq < Lk, bottom-right causal, ALiBi
+    (20, 20, True, 4, True),     # GQA: dK, dV summed over the group
+])
+def test_backward_matches_torch_autograd_fp64(Lq, Lk, causal, G, alibi):
+    from oracle import attention_backward_ref
+    B, Hkv, d, s = 2, 2, 8, 0.6
+    Hq = Hkv * G
+    q = _rand(B, Hq, Lq, d)
+    k = _rand(B, Hkv, Lk, d)
+    v = _rand(B, Hkv, Lk, d)
+    g = _rand(B, Hq, Lq, d)
+    slopes = np.array([2.0 ** (-8.0 * (h + 1) / Hq) for h in range(Hq)])
+    mask = np.zeros((1, Hq, Lq, Lk))
+    for h in range(Hq):
+        for i in range(Lq):
+            for j in range(Lk):
+                ia = i + Lk - Lq
+                val = -slopes[h] * abs(ia - j) if alibi else 0.0
+                if causal and j > ia:
+                    val = -math.inf
+                mask[0, h, i, j] = val
+    tq = torch.tensor(q, requires_grad=True)
+    tk = torch.tensor(k, requires_grad=True)
+    tv = torch.tensor(v, requires_grad=True)
+    out = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk.repeat_interleave(G, dim=1), tv.repeat_interleave(G, dim=1),
+        attn_mask=torch.tensor(mask), scale=s)
+    out.backward(torch.tensor(g))
+    dQ, dK, dV = attention_backward_ref(q, k, v, g, scale=s, causal=causal,
+                                        alibi_slopes=slopes if alibi else None)
+    assert np.max(np.abs(dQ - tq.grad.numpy())) < 1e-11
+    assert np.max(np.abs(dK - tk.grad.numpy())) < 1e-11
+    assert np.max(np.abs(dV - tv.grad.numpy())) < 1e-11
+
+
+def test_backward_finite_differences_tiny():
+    """Central differences of L = sum(dO * O) with the oracle's own forward
+    (brute force on a 2-head, 5-row problem)."""
+    from oracle import attention_backward_ref
+    q = _rand(1, 2, 5, 3)
+    k = _rand(1, 1, 5, 3)
+    v = _rand(1, 1, 5, 3)
+    g = _rand(1, 2, 5, 3)
+    s = 0.8
+
+    def loss(q_, k_, v_):
+        O, _ = attention_ref(q_, k_, v_, scale=s, causal=True)
+        return float((O * g).sum())
+
+    dQ, dK, dV = attention_backward_ref(q, k, v, g, scale=s, causal=True)
+    eps = 1e-6
+    for arr, grad in ((q, dQ), (k, dK), (v, dV)):
+        for idx in [(0, 0, 0, 0), (0, 0, 3, 2), (0, arr.shape[1] - 1, 4, 1)]:
+            plus, minus = arr.copy(), arr.copy()
+            plus[idx] += eps
+            minus[idx] -= eps
+            args_p = [plus if a is arr else a for a in (q, k, v)]
+            args_m = [minus if a is arr else a for a in (q, k, v)]
+            num = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(num - grad[idx]) < 1e-7, (idx, num, grad[idx])
+
+
+def test_backward_value_gradient_is_probability_weighted():
+    """dV_j = sum_i P_ij dO_i: with dO = 1 every dV row is the column sum of
+    P, and those sums add up to the number of rows that see a key."""
+    from oracle import attention_backward_ref
+    q = _rand(1, 1, 11, 4)
+    k = _rand(1, 1, 11, 4)
+    v = _rand(1, 1, 11, 4)
+    g = np.ones((1, 1, 11, 4))
+    _, _, dV = attention_backward_ref(q, k, v, g, scale=0.5, causal=True)
+    assert abs(dV[0, 0, :, 0].sum() - 11.0) < 1e-12
+    # the last key is seen only by the last row, with its probability
+    O, L = attention_ref(q, k, v, scale=0.5, causal=True)
+    p_last = math.exp(0.5 * float(q[0, 0, 10] @ k[0, 0, 10]) - L[0, 0, 10])
+    assert abs(dV[0, 0, 10, 0] - p_last) < 1e-12
