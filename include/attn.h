@@ -125,6 +125,33 @@ int attn_prefill_opts(const void* Q, const void* K, const void* V,
                       const attn_prefill_options* opts, void* stream);
 
 /*
+ * attn_backward - gradients of attn_prefill (causal / ALiBi / GQA variants).
+ *
+ * The single-pass backward the Twill review (xllm-io) describes in §七 7.2:
+ * per K/V block, recompute P = exp(x - LSE) from the forward's LSE, then
+ *   dV = P^T dO,  dP = dO V^T,  dS = P (dP - rowsum(dO * O)),
+ *   dQ = s dS K (accumulated across K/V blocks with fp32 atomics),
+ *   dK = s dS^T Q;  dK and dV are summed over the query heads of a GQA group.
+ *
+ *   Q, O, dO bf16 [B, Hq, Lq, d]; K, V bf16 [B, Hkv, Lk, d]   (device, read)
+ *   LSE      fp32 [B, Hq, Lq] from attn_prefill               (device, read)
+ *   dQ       bf16 [B, Hq, Lq, d]; dK, dV bf16 [B, Hkv, Lk, d] (device, written)
+ *   causal, scale, alibi_slopes as in attn_prefill (softcap / window: not
+ *            supported here).
+ *   workspace  device scratch of attn_backward_workspace_bytes(B, Hq, Lq, d)
+ *            bytes, 16-byte aligned, owned by the caller (fp32 dQ accumulator
+ *            and the row sums); its contents on entry do not matter.
+ */
+size_t attn_backward_workspace_bytes(int B, int Hq, int Lq, int d);
+
+int attn_backward(const void* Q, const void* K, const void* V,
+                  const void* O, const void* dO, const float* LSE,
+                  void* dQ, void* dK, void* dV,
+                  int B, int Hq, int Hkv, int Lq, int Lk, int d,
+                  int causal, float scale, const float* alibi_slopes,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Split-K decode (Neptune论文浅读 §6; the split-KV decode of CMU 15-779
  * 第 11 讲 §7.1, which parallelises over batch x KV head x KV sequence and
  * stacks the G = Hq / Hkv query heads of a group as rows so that each K/V row

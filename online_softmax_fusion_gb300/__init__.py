@@ -44,6 +44,9 @@ SIGNATURES = {
                                                                    _c_void_p]),
     "attn_prefill_opts": (_c_int, [_c_void_p] * 5 + [_c_int] * 6 + [ctypes.POINTER(PrefillOptions),
                                                                      _c_void_p]),
+    "attn_backward_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
+    "attn_backward": (_c_int, [_c_void_p] * 9 + [_c_int] * 7 + [_c_float, _c_void_p, _c_void_p,
+                                                               ctypes.c_size_t, _c_void_p]),
     "attn_decode_num_splits": (_c_int, [_c_int] * 5),
     "attn_decode_split_len": (_c_int, [_c_int] * 2),
     "attn_decode_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
@@ -147,6 +150,35 @@ def prefill(q, k, v, causal=False, scale=None, alibi_slopes=None, impl="auto", o
                                    IMPLS[impl], _stream())
     _check(st, "attn_prefill")
     return out, lse
+
+
+def backward(q, k, v, o, lse, dout, causal=False, scale=None, alibi_slopes=None,
+             workspace=None):
+    """Gradients of prefill: returns (dQ, dK, dV) bf16; dK and dV are per KV
+    head (summed over a GQA group). `lse` is the forward's fp32 LSE."""
+    for t, n in ((q, "q"), (o, "o"), (dout, "dout")):
+        _req(t, n, torch.bfloat16, 4)
+    _req(k, "k", torch.bfloat16, 4)
+    _req(v, "v", torch.bfloat16, 4)
+    _req(lse, "lse", torch.float32, 3)
+    B, Hq, Lq, d = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if alibi_slopes is not None:
+        _req(alibi_slopes, "alibi_slopes", torch.float32, 1)
+    nbytes = lib().attn_backward_workspace_bytes(B, Hq, Lq, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes // 4, dtype=torch.float32, device=q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    st = lib().attn_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                             _ptr(dk), _ptr(dv), B, Hq, Hkv, Lq, Lk, d, int(bool(causal)),
+                             float(scale), _ptr(alibi_slopes), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream())
+    _check(st, "attn_backward")
+    return dq, dk, dv
 
 
 def resolve_splits(B, Hkv, Lk_max, d, requested=0) -> int:

@@ -234,6 +234,55 @@ int attn_prefill(const void* Q, const void* K, const void* V, void* O, float* LS
                            ATTN_IMPL_AUTO, stream);
 }
 
+size_t attn_backward_workspace_bytes(int B, int Hq, int Lq, int d) {
+    if (B <= 0 || Hq <= 0 || Lq <= 0 || d <= 0) return 0;
+    const size_t rows = size_t(B) * size_t(Hq) * size_t(Lq);
+    return rows * size_t(d) * sizeof(float) + rows * sizeof(float);
+}
+
+int attn_backward(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                  const float* LSE, void* dQ, void* dK, void* dV, int B, int Hq, int Hkv, int Lq,
+                  int Lk, int d, int causal, float scale, const float* alibi_slopes,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+    if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
+        return ATTN_ERR_NULL;
+    int st = check_common(B, Hq, Hkv, d, scale);
+    if (st) return st;
+    if (Lq <= 0 || Lk <= 0) return ATTN_ERR_SHAPE;
+    const void* ptrs[] = {Q, K, V, O, dO, dQ, dK, dV, workspace};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return ATTN_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(LSE) & 3u) ||
+        (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)))
+        return ATTN_ERR_ALIGN;
+    if (workspace_bytes < attn_backward_workspace_bytes(B, Hq, Lq, d)) return ATTN_ERR_WORKSPACE;
+    BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.Q = static_cast<const __nv_bfloat16*>(Q);
+    p.K = static_cast<const __nv_bfloat16*>(K);
+    p.V = static_cast<const __nv_bfloat16*>(V);
+    p.O = static_cast<const __nv_bfloat16*>(O);
+    p.dO = static_cast<const __nv_bfloat16*>(dO);
+    p.LSE = LSE;
+    p.dQ = static_cast<__nv_bfloat16*>(dQ);
+    p.dK = static_cast<__nv_bfloat16*>(dK);
+    p.dV = static_cast<__nv_bfloat16*>(dV);
+    p.dQacc = static_cast<float*>(workspace);
+    p.Dsum = p.dQacc + size_t(B) * Hq * Lq * d;
+    p.slopes = alibi_slopes;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Lq = Lq;
+    p.Lk = Lk;
+    p.G = Hq / Hkv;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.causal = causal ? 1 : 0;
+    if ((long long)(Lk + 63) / 64 > 0x7fffffffLL || Hkv > 65535) return ATTN_ERR_SHAPE;
+    return launch_backward(p, d, static_cast<cudaStream_t>(stream));
+}
+
 int attn_decode_split_len(int Lk_max, int num_splits) {
     if (Lk_max <= 0) return -ATTN_ERR_SHAPE;
     if (num_splits <= 0) return -ATTN_ERR_WORKSPACE;

@@ -52,6 +52,20 @@ struct PrefillLaunch {
     PrefillParams p;
 };
 
+struct BwdParams {
+    const __nv_bfloat16 *Q, *K, *V, *O, *dO;   // forward tensors and dO (layouts as forward)
+    const float* LSE;                         // [B, Hq, Lq] natural-log LSE of the forward
+    __nv_bfloat16 *dQ, *dK, *dV;              // gradients (dK, dV per KV head)
+    float* dQacc;                             // fp32 [B, Hq, Lq, d] accumulator (workspace)
+    float* Dsum;                              // fp32 [B, Hq, Lq] rowsum(dO * O) (workspace)
+    const float* slopes;                      // [Hq] or nullptr (ALiBi)
+    int B, Hq, Hkv, Lq, Lk, G;
+    float scale, scale_log2;
+    int causal;
+};
+
+int launch_backward(const BwdParams& p, int d, cudaStream_t stream);
+
 int launch_decode(const DecodeLaunch& L, int d, cudaStream_t stream);
 int launch_combine(const float* O_part, const float* LSE_part, int B, int Hq, int S, int d,
                    void* O, float* LSE, cudaStream_t stream);

@@ -129,3 +129,17 @@ def test_binding_rejects_cpu_tensors(L):
     q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         attn.prefill(q, q, q)
+
+
+def test_backward_validation_before_launch(L):
+    def bwd(Q=P, K=P, V=P, O=P, dO=P, LSE=P, dQ=P, dK=P, dV=P, B=1, Hq=4, Hkv=2, Lq=128, Lk=128,
+            d=128, causal=1, scale=0.1, ws=P, wsb=1 << 30):
+        return L.attn_backward(Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, Lq, Lk, d, causal,
+                               scale, None, ws, wsb, None)
+    assert bwd(dO=None) == 1
+    assert bwd(ws=None) == 1
+    assert bwd(Hq=3) == 2
+    assert bwd(d=96) == 3
+    assert bwd(wsb=16) == 4
+    assert bwd(dK=MIS) == 7
+    assert L.attn_backward_workspace_bytes(2, 4, 100, 128) == 2 * 4 * 100 * 129 * 4
