@@ -63,6 +63,12 @@ def prefill_flops(B, Hq, Lq, Lk, d, causal) -> int:
     return 4 * d * B * Hq * pairs
 
 
+def backward_flops(B, Hq, Lq, Lk, d, causal) -> int:
+    """Five products per unmasked pair (S recomputed, dP, dV, dK, dQ): 10*d."""
+    pairs = causal_pairs(Lq, Lk) if causal else Lq * Lk
+    return 10 * d * B * Hq * pairs
+
+
 def prefill_io_bytes(B, Hq, Hkv, Lq, Lk, d, elem=2) -> int:
     """Q read, O written, K and V read once per KV head (fused kernel)."""
     return 2 * B * Hq * Lq * d * elem + 2 * B * Hkv * Lk * d * elem
@@ -290,6 +296,23 @@ def measure_other_workloads(attn, W, dev, peaks):
         sweep.append({"L": L, "ms": ms, "tflops": tf, "frac": tf / peaks["bf16_tflops"],
                       "inputs_exceed_l2": in_bytes > 129e6, "timing": "cuda graph replay"})
         del inp, O, LSE
+    # backward of the causal MHA workload (forward outputs as its inputs)
+    pc = W.PREFILL_CONFIGS[PREFILL_WORKLOAD]
+    pin = W.make_prefill_inputs(pc, dev)
+    g = W.seeded_generator(pc.seed + 7, dev)
+    dout = W._normal_bf16(pin["q"].shape, g, dev)
+    O, LSE = attn.prefill(pin["q"], pin["k"], pin["v"], causal=True, scale=pc.scale)
+    ws = torch.empty(attn.lib().attn_backward_workspace_bytes(pc.B, pc.Hq, pc.Lq, pc.d) // 4,
+                     dtype=torch.float32, device=dev)
+    t_bwd = time_launches(lambda: attn.backward(pin["q"], pin["k"], pin["v"], O, LSE, dout,
+                                                causal=True, scale=pc.scale, workspace=ws),
+                          5, 2, stream)
+    bfl = backward_flops(pc.B, pc.Hq, pc.Lq, pc.Lk, pc.d, True)
+    bwd = {"workload": PREFILL_WORKLOAD + " backward", "ms": t_bwd,
+           "tflops": bfl / (t_bwd * 1e-3) / 1e12,
+           "frac": bfl / (t_bwd * 1e-3) / 1e12 / peaks["bf16_tflops"],
+           "flops": bfl, "kernels": "prep + main (mma.sync) + convert"}
+    del pin, dout, O, LSE, ws
     dc = W.DECODE_CONFIGS["decode_long_outlier"]
     din = W.make_decode_inputs(dc, dev)
     S = attn.resolve_splits(dc.B, dc.Hkv, dc.Lk_max, dc.d, dc.num_splits)
@@ -307,7 +330,8 @@ def measure_other_workloads(attn, W, dev, peaks):
                 "kv_gbs": gbs, "path_gbs": kvb / ((t_dec + t_cmb) * 1e-3) / 1e9,
                 "frac": gbs / peaks["hbm_gbs"], "kv_bytes": kvb}
     del din, Op, Lp, Od, Ld
-    return {"prefill_gqa_alibi_sweep": sweep, "decode_long_outlier": long_dec}
+    return {"prefill_gqa_alibi_sweep": sweep, "decode_long_outlier": long_dec,
+            "backward_causal_mha_4k": bwd}
 
 
 # ------------------------------------------------------------ CPU oracle

@@ -114,3 +114,8 @@ def test_clock_summary_keeps_only_samples_inside_the_region():
     c = bench.ClockSampler.summarize(lines, t0, t1)
     assert c["samples_in_region"] == 2 and c["sm_mhz"] == 1490.0
     assert c["reasons"] == ["sw_power_cap"] and c["sm_max_mhz"] == 2070.0
+
+
+def test_backward_flops_are_two_and_a_half_forward():
+    assert bench.backward_flops(2, 3, 100, 130, 64, True) * 2 == \
+        5 * bench.prefill_flops(2, 3, 100, 130, 64, True)
