@@ -5,8 +5,9 @@ CPU-baseline / reference arm may import this package. The product path (the
 CUDA library and its Python binding) never imports, calls or links anything
 here, and this package imports nothing from the product.
 
-Pinned by tests/test_oracle_pins.py (closed forms, invariants, a library
-special case and brute force on tiny inputs). Every public function is pinned.
+Pinned by tests/test_oracle_pins.py and tests/test_oracle_rmsnorm_pins.py
+(closed forms, invariants, library special cases and brute force on tiny
+inputs). Every public function is pinned.
 """
 from .attention import (  # noqa: F401
     attend_head,
@@ -18,4 +19,13 @@ from .attention import (  # noqa: F401
     online_softmax_rolling,
     naive_fused_exp_sum,
     repair,
+)
+from .rmsnorm import (  # noqa: F401
+    rms_ref,
+    rmsnorm_ref,
+    rmsnorm_matmul_ref,
+    sumsq_repair,
+    sumsq_rolling,
+    sumsq_combine,
+    l2norm_stable,
 )

@@ -12,9 +12,15 @@ forward-attention benchmark shape of the Twill review (xllm-io) §七
 CMU 15-779 第 11 讲 §7.1 (query heads stacked per KV head). The pages measure
 on no dataset; inputs are i.i.d. normal bf16 values from a fixed seed.
 
+The RMSNorm + MatMul workload takes the LLaMA-2-7B shape of CMU 15-779
+第 11 讲 §3.3 (hidden H = output D = 4096) at a small batch and at batch 256.
+X is N(0, 1), the RMSNorm weight G is 1 + 0.1 N(0, 1) and W is N(0, 1) / sqrt(H)
+(so O has unit scale), all rounded to bf16.
+
 Layout of every tensor (row-major, innermost dimension last):
   prefill  Q [B, Hq, Lq, d], K and V [B, Hkv, Lk, d]
   decode   Q [B, Hq, d],     K and V [B, Hkv, Lk_max, d], kv_lens [B] int32
+  rmsnorm  X [B, H], G [H], W [H, D], O [B, D]
 """
 from __future__ import annotations
 
@@ -27,7 +33,7 @@ __all__ = [
     "PrefillConfig", "DecodeConfig", "PREFILL_CONFIGS", "DECODE_CONFIGS",
     "GQA_SWEEP_LENGTHS", "gqa_sweep_config", "alibi_slopes",
     "make_prefill_inputs", "make_decode_inputs", "seeded_generator",
-    "sample_rows",
+    "sample_rows", "RmsMatmulConfig", "RMS_MATMUL_CONFIGS", "make_rmsnorm_matmul_inputs",
 ]
 
 
@@ -104,6 +110,25 @@ DECODE_CONFIGS = {
 }
 
 
+@dataclass(frozen=True)
+class RmsMatmulConfig:
+    name: str
+    B: int
+    H: int
+    D: int
+    seed: int = 0
+
+
+RMS_MATMUL_CONFIGS = {
+    "rmsnorm_matmul_small_ragged": RmsMatmulConfig(
+        "rmsnorm_matmul_small_ragged", B=5, H=328, D=200, seed=1300),
+    "rmsnorm_matmul_llama7b_b16": RmsMatmulConfig(
+        "rmsnorm_matmul_llama7b_b16", B=16, H=4096, D=4096, seed=1301),
+    "rmsnorm_matmul_llama7b_b256": RmsMatmulConfig(
+        "rmsnorm_matmul_llama7b_b256", B=256, H=4096, D=4096, seed=1302),
+}
+
+
 def seeded_generator(seed: int, device) -> torch.Generator:
     g = torch.Generator(device=torch.device(device))
     g.manual_seed(int(seed))
@@ -173,3 +198,13 @@ def sample_rows(L: int, n_random: int, n_edge: int, seed: int) -> torch.Tensor:
     if n_random > 0:
         parts.append(torch.randint(0, L, (n_random,), generator=g))
     return torch.unique(torch.cat(parts)).to(torch.int64)
+
+
+def make_rmsnorm_matmul_inputs(cfg: RmsMatmulConfig, device="cpu", seed: int | None = None):
+    """X [B, H] ~ N(0, 1), G [H] ~ 1 + 0.1 N(0, 1), W [H, D] ~ N(0, 1) / sqrt(H); bf16."""
+    dev = torch.device(device)
+    g = seeded_generator(cfg.seed if seed is None else seed, dev)
+    x = _normal_bf16((cfg.B, cfg.H), g, dev)
+    gw = (1.0 + 0.1 * torch.randn(cfg.H, generator=g, device=dev)).to(torch.bfloat16)
+    w = (torch.randn(cfg.H, cfg.D, generator=g, device=dev) / math.sqrt(cfg.H)).to(torch.bfloat16)
+    return {"x": x, "g": gw, "w": w}
