@@ -69,6 +69,15 @@ def backward_flops(B, Hq, Lq, Lk, d, causal) -> int:
     return 10 * d * B * Hq * pairs
 
 
+def rmsnorm_matmul_bytes(B, H, D) -> int:
+    """Algorithmic bytes of O = RMSNorm(X; G) W: W, X and G read once, O written once (bf16)."""
+    return 2 * (H * D + B * H + H + B * D)
+
+
+def rmsnorm_matmul_flops(B, H, D) -> int:
+    return 2 * B * H * D
+
+
 def prefill_io_bytes(B, Hq, Hkv, Lq, Lk, d, elem=2) -> int:
     """Q read, O written, K and V read once per KV head (fused kernel)."""
     return 2 * B * Hq * Lq * d * elem + 2 * B * Hkv * Lk * d * elem
@@ -330,8 +339,31 @@ def measure_other_workloads(attn, W, dev, peaks):
                 "kv_gbs": gbs, "path_gbs": kvb / ((t_dec + t_cmb) * 1e-3) / 1e9,
                 "frac": gbs / peaks["hbm_gbs"], "kv_bytes": kvb}
     del din, Op, Lp, Od, Ld
+    # fused RMSNorm + product at the LLaMA-2-7B shape (H = D = 4096): the calls
+    # cycle through 5 copies of W (5 x 32 MB > L2), so each reads W from HBM
+    rms = []
+    for name in ("rmsnorm_matmul_llama7b_b16", "rmsnorm_matmul_llama7b_b256"):
+        cfg = W.RMS_MATMUL_CONFIGS[name]
+        rin = W.make_rmsnorm_matmul_inputs(cfg, dev)
+        wcopies = [rin["w"]] + [rin["w"].clone() for _ in range(4)]
+        Orm = torch.empty((cfg.B, cfg.D), dtype=torch.bfloat16, device=dev)
+
+        def fn_rms():
+            for wc in wcopies:
+                attn.rmsnorm_matmul(rin["x"], rin["g"], wc, out=Orm)
+        ms = graph_time(fn_rms, 4, replays=5) / len(wcopies)
+        byts = rmsnorm_matmul_bytes(cfg.B, cfg.H, cfg.D)
+        fl = rmsnorm_matmul_flops(cfg.B, cfg.H, cfg.D)
+        gbs = byts / (ms * 1e-3) / 1e9
+        tf = fl / (ms * 1e-3) / 1e12
+        rms.append({"workload": name, "B": cfg.B, "H": cfg.H, "D": cfg.D, "ms": ms,
+                    "gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "tflops": tf,
+                    "frac_bf16": tf / peaks["bf16_tflops"], "bytes": byts, "flops": fl,
+                    "splits": attn.lib().attn_rmsnorm_matmul_splits(cfg.B, cfg.H, cfg.D),
+                    "timing": "cuda graph replay, W rotated over 5 copies (> L2)"})
+        del rin, wcopies, Orm
     return {"prefill_gqa_alibi_sweep": sweep, "decode_long_outlier": long_dec,
-            "backward_causal_mha_4k": bwd}
+            "backward_causal_mha_4k": bwd, "rmsnorm_matmul": rms}
 
 
 # ------------------------------------------------------------ CPU oracle

@@ -152,6 +152,54 @@ int attn_backward(const void* Q, const void* K, const void* V,
                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_rmsnorm_matmul - RMSNorm followed by a matrix product, fused into one
+ * kernel.
+ *
+ *   O = RMSNorm(X; G) W = ((X ⊙ G) W) / RMS(X),
+ *   RMS(X)_i = sqrt( (1/H) sum_j X_ij^2 + eps )
+ *
+ * 第 11 讲 · 高级 ML 编译 (CMU 15-779) §3: the division by RMS commutes with
+ * the product and moves after it, and the two reductions over the hidden
+ * dimension (sum of squares, product) run in one loop. The sum of squares is
+ * the numerically stable one (Neptune论文浅读 §4's repair for the L2 norm:
+ * a running power-of-two reference above max |x| and the sum of the scaled
+ * squares, repaired when the reference grows), so rows far beyond
+ * sqrt(FLT_MAX) in magnitude keep a finite RMS.
+ *
+ *   X    bf16 [B, H] row-major                 (device, read)
+ *   G    bf16 [H]                              (device, read)
+ *   W    bf16 [H, D] row-major                 (device, read)
+ *   O    bf16 [B, D] row-major                 (device, written)
+ *   rms  fp32 [B] RMS(X) per row, or NULL      (device, written)
+ *   eps  >= 0 and finite; the page's RMS has none (pass 0 for it)
+ *   splits  CTAs that split the hidden dimension for one output tile and
+ *           reduce through distributed shared memory (a thread-block
+ *           cluster): 1, 2, 4 or 8, at most ceil(H / 64); 0 lets the library
+ *           choose (attn_rmsnorm_matmul_splits).
+ * A row whose RMS is 0 (all zeros, eps = 0) gives a zero output row.
+ * Requirements: H and D multiples of 8 (16-byte row strides); X, G, W, O
+ * 16-byte aligned. Errors: ATTN_ERR_NULL (X, G, W or O NULL), ATTN_ERR_SHAPE
+ * (a size <= 0 or too large), ATTN_ERR_UNSUPPORTED (H or D not a multiple of
+ * 8), ATTN_ERR_VALUE (eps negative or not finite, bad split count),
+ * ATTN_ERR_ALIGN; nothing is launched then. Asynchronous on `stream`;
+ * allocates nothing.
+ */
+int attn_rmsnorm_matmul(const void* X, const void* G, const void* W, void* O, float* rms,
+                        int B, int H, int D, float eps, int splits, void* stream);
+
+/* The same with the batch tile chosen by the caller: batch_tile rows of X per
+ * CTA (a multiple of 16, at most 256; 0 = the library's choice, one tile when
+ * B <= 256). Smaller tiles give more CTAs without a K split; larger tiles
+ * stream W fewer times. ATTN_ERR_VALUE for any other batch_tile. */
+int attn_rmsnorm_matmul_tiled(const void* X, const void* G, const void* W, void* O, float* rms,
+                              int B, int H, int D, float eps, int batch_tile, int splits,
+                              void* stream);
+
+/* The split count attn_rmsnorm_matmul chooses when given 0 (negative status on
+ * invalid sizes). */
+int attn_rmsnorm_matmul_splits(int B, int H, int D);
+
+/*
  * Split-K decode (Neptune论文浅读 §6; the split-KV decode of CMU 15-779
  * 第 11 讲 §7.1, which parallelises over batch x KV head x KV sequence and
  * stacks the G = Hq / Hkv query heads of a group as rows so that each K/V row

@@ -47,6 +47,11 @@ SIGNATURES = {
     "attn_backward_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
     "attn_backward": (_c_int, [_c_void_p] * 9 + [_c_int] * 7 + [_c_float, _c_void_p, _c_void_p,
                                                                ctypes.c_size_t, _c_void_p]),
+    "attn_rmsnorm_matmul": (_c_int, [_c_void_p] * 5 + [_c_int] * 3 + [_c_float, _c_int,
+                                                                     _c_void_p]),
+    "attn_rmsnorm_matmul_tiled": (_c_int, [_c_void_p] * 5 + [_c_int] * 3 + [_c_float, _c_int,
+                                                                           _c_int, _c_void_p]),
+    "attn_rmsnorm_matmul_splits": (_c_int, [_c_int] * 3),
     "attn_decode_num_splits": (_c_int, [_c_int] * 5),
     "attn_decode_split_len": (_c_int, [_c_int] * 2),
     "attn_decode_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
@@ -179,6 +184,28 @@ def backward(q, k, v, o, lse, dout, causal=False, scale=None, alibi_slopes=None,
                              workspace.numel() * workspace.element_size(), _stream())
     _check(st, "attn_backward")
     return dq, dk, dv
+
+
+def rmsnorm_matmul(x, g, w, eps=0.0, splits=0, out=None, rms=None, with_rms=False,
+                   batch_tile=0):
+    """Fused RMSNorm + product: O = ((x * g) @ w) / RMS(x), RMS(x) =
+    sqrt(mean(x^2) + eps). x [B,H], g [H], w [H,D] bf16 CUDA. Returns
+    (O bf16 [B,D], RMS fp32 [B] or None). batch_tile / splits: 0 = auto."""
+    _req(x, "x", torch.bfloat16, 2)
+    _req(g, "g", torch.bfloat16, 1)
+    _req(w, "w", torch.bfloat16, 2)
+    B, H = x.shape
+    D = w.shape[1]
+    if g.shape[0] != H or w.shape[0] != H:
+        raise ValueError("g must be [H] and w [H, D] matching x [B, H]")
+    if out is None:
+        out = torch.empty((B, D), dtype=torch.bfloat16, device=x.device)
+    if rms is None and with_rms:
+        rms = torch.empty((B,), dtype=torch.float32, device=x.device)
+    st = lib().attn_rmsnorm_matmul_tiled(_ptr(x), _ptr(g), _ptr(w), _ptr(out), _ptr(rms), B, H,
+                                         D, float(eps), int(batch_tile), int(splits), _stream())
+    _check(st, "attn_rmsnorm_matmul")
+    return out, rms
 
 
 def resolve_splits(B, Hkv, Lk_max, d, requested=0) -> int:

@@ -1,6 +1,7 @@
 // C-ABI layer of libattn.so: argument validation, TMA descriptor encoding,
 // split-count policy, launch dispatch and the device status word.
 // The entry points are declared and documented in include/attn.h.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -92,6 +93,42 @@ int check_common(int B, int Hq, int Hkv, int d, float scale) {
 
 int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
 
+// Tile geometry of the fused RMSNorm + product: batch rows per CTA (one tile
+// when B <= 256, else equal tiles of at most 256), ring depth (about 100 KB so
+// two CTAs can share an SM when the batch tile is small) and the K split:
+// the largest power of two <= 8 that keeps every CTA resident at once and
+// gives each at least one 64-wide K step.
+struct RmsGeometry {
+    int NB, stages, splits, k_tiles, cvt_warps, cvt_groups;
+};
+
+RmsGeometry rms_geometry(int B, int H, int D, int splits_req, int tile_req, bool query_device) {
+    RmsGeometry g;
+    const int tile_max = tile_req > 0 ? tile_req : 256;
+    const int b_tiles = ceil_div(B, tile_max);
+    g.NB = ceil_div(ceil_div(B, b_tiles), 16) * 16;
+    const int stage_bytes = 16384 + g.NB * 128;
+    g.stages = std::max(3, std::min(kRmsMaxStages, 102400 / stage_bytes));
+    // converter warps per K step: one thread per batch row; the groups that
+    // fit in the 8 converter warps own ring slots in turn, so the ring depth
+    // is rounded down to a multiple of their count
+    g.cvt_warps = ceil_div(g.NB, 32);
+    g.cvt_groups = std::min(8 / g.cvt_warps, g.stages);
+    g.stages = std::max(g.cvt_groups, g.stages / g.cvt_groups * g.cvt_groups);
+    g.k_tiles = ceil_div(H, 64);
+    if (splits_req > 0) {
+        g.splits = splits_req;
+        return g;
+    }
+    const long long base = (long long)ceil_div(D, 128) * ceil_div(B, g.NB);
+    const long long slots =
+        (long long)sm_count() * (query_device ? rmsnorm_matmul_blocks_per_sm(g.NB, g.stages) : 1);
+    g.splits = 1;
+    while (g.splits * 2 <= 8 && g.splits * 2 <= g.k_tiles && base * g.splits * 2 <= slots)
+        g.splits *= 2;
+    return g;
+}
+
 }  // namespace
 
 // One thread waits on a barrier that nothing arrives on, with a short limit:
@@ -125,7 +162,7 @@ const char* attn_status_string(int status) {
         case ATTN_ERR_CUDA: return "a CUDA call failed";
         case ATTN_ERR_TIMEOUT: return "a device wait exceeded its time limit";
         case ATTN_ERR_ALIGN: return "pointer not 16-byte aligned";
-        case ATTN_ERR_VALUE: return "invalid value (scale not finite)";
+        case ATTN_ERR_VALUE: return "invalid value (non-finite scale or eps, or a bad split count)";
         default: return "unknown status";
     }
 }
@@ -281,6 +318,57 @@ int attn_backward(const void* Q, const void* K, const void* V, const void* O, co
     p.causal = causal ? 1 : 0;
     if ((long long)(Lk + 63) / 64 > 0x7fffffffLL || Hkv > 65535) return ATTN_ERR_SHAPE;
     return launch_backward(p, d, static_cast<cudaStream_t>(stream));
+}
+
+int attn_rmsnorm_matmul_splits(int B, int H, int D) {
+    if (B <= 0 || H <= 0 || D <= 0) return -ATTN_ERR_SHAPE;
+    int dev = 0;
+    const bool have_dev = cudaGetDevice(&dev) == cudaSuccess;
+    return rms_geometry(B, H, D, 0, 0, have_dev).splits;
+}
+
+int attn_rmsnorm_matmul(const void* X, const void* G, const void* W, void* O, float* rms, int B,
+                        int H, int D, float eps, int splits, void* stream) {
+    return attn_rmsnorm_matmul_tiled(X, G, W, O, rms, B, H, D, eps, 0, splits, stream);
+}
+
+int attn_rmsnorm_matmul_tiled(const void* X, const void* G, const void* W, void* O, float* rms,
+                              int B, int H, int D, float eps, int batch_tile, int splits,
+                              void* stream) {
+    if (!X || !G || !W || !O) return ATTN_ERR_NULL;
+    if (B <= 0 || H <= 0 || D <= 0) return ATTN_ERR_SHAPE;
+    if (B > 65535 * 256 || H > (1 << 30) || D > (1 << 30)) return ATTN_ERR_SHAPE;
+    if (H % 8 != 0 || D % 8 != 0) return ATTN_ERR_UNSUPPORTED;
+    if (!std::isfinite(eps) || eps < 0.f) return ATTN_ERR_VALUE;
+    if (!(splits == 0 || splits == 1 || splits == 2 || splits == 4 || splits == 8))
+        return ATTN_ERR_VALUE;
+    if (splits > 0 && splits > ceil_div(H, 64)) return ATTN_ERR_VALUE;
+    if (batch_tile < 0 || batch_tile > 256 || batch_tile % 16) return ATTN_ERR_VALUE;
+    const void* ptrs[] = {X, G, W, O};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return ATTN_ERR_ALIGN;
+    if (rms && (reinterpret_cast<uintptr_t>(rms) & 3u)) return ATTN_ERR_ALIGN;
+    const RmsGeometry g = rms_geometry(B, H, D, splits, batch_tile, true);
+    RmsLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    L.p.O = static_cast<__nv_bfloat16*>(O);
+    L.p.rms = rms;
+    L.p.G = static_cast<const __nv_bfloat16*>(G);
+    L.p.B = B;
+    L.p.H = H;
+    L.p.D = D;
+    L.p.NB = g.NB;
+    L.p.splits = g.splits;
+    L.p.k_tiles = g.k_tiles;
+    L.p.stages = g.stages;
+    L.p.cvt_warps = g.cvt_warps;
+    L.p.cvt_groups = g.cvt_groups;
+    L.p.eps = eps;
+    L.p.status = status_ptr();
+    int st;
+    if ((st = make_map(&L.tmX, X, H, B, 1, g.NB))) return st;
+    if ((st = make_map(&L.tmW, W, D, H, 1, 64))) return st;
+    return launch_rmsnorm_matmul(L, static_cast<cudaStream_t>(stream));
 }
 
 int attn_decode_split_len(int Lk_max, int num_splits) {

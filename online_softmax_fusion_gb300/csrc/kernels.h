@@ -81,4 +81,29 @@ constexpr int kTcBM = 128;
 constexpr int kTcBN = 128;
 int launch_prefill_tc(const PrefillLaunch& L, int d, cudaStream_t stream);
 
+// Fused RMSNorm + matrix product: X [B, H], G [H], W [H, D] -> O [B, D].
+struct RmsParams {
+    __nv_bfloat16* O;                         // [B, D]
+    float* rms;                               // [B] or nullptr
+    const __nv_bfloat16* G;                   // [H]
+    int B, H, D;
+    int NB;                                   // batch rows per CTA (multiple of 16, <= 256)
+    int splits;                               // CTAs of a cluster sharing one output tile (K split)
+    int k_tiles;                              // ceil(H / 64)
+    int stages;                               // ring depth
+    int cvt_warps;                            // converter warps per K step (<= 8)
+    int cvt_groups;                           // groups taking K steps in turn; divides stages
+    float eps;
+    int* status;
+};
+
+struct RmsLaunch {
+    CUtensorMap tmX, tmW;
+    RmsParams p;
+};
+
+constexpr int kRmsMaxStages = 8;
+int launch_rmsnorm_matmul(const RmsLaunch& L, cudaStream_t stream);
+int rmsnorm_matmul_blocks_per_sm(int NB, int stages);   // 1 when no device answers
+
 }  // namespace attn

@@ -1,0 +1,571 @@
+// Fused RMSNorm + matrix product on the 5th-generation tensor cores:
+//
+//   O = ((X ⊙ G) W) / RMS(X),   RMS(X)_i = sqrt(mean_j X_ij^2 + eps)
+//
+// 第 11 讲 · 高级 ML 编译 (CMU 15-779) §3 describes the fusion: the division
+// by RMS commutes with the product, so it moves after it, and the two
+// reductions along the hidden dimension (sum of squares, and the product)
+// run in the same loop with their partial sums kept on chip; the scalar tail
+// (constant, square root, division) is element-wise work in registers.
+//
+// The sum of squares is the numerically stable one with the repair that
+// Neptune论文浅读 (gentlecold.top) §4 derives for the L2 norm: each row keeps
+// a reference 2^E above its largest |x| and the sum s of (x 2^-E)^2; when a
+// tile raises E, s is repaired by 2^(2 (E_old - E_new)). With power-of-two
+// references the scaling and the repair are exact, and no x^2 is formed, so
+// inputs far beyond sqrt(FLT_MAX) keep a finite RMS. Across the K split the
+// partial (E, s) of each CTA merge against the largest E (§6's pattern).
+//
+// Shapes: X [B, H] and O [B, D] row-major, G [H], W [H, D] row-major (O = Y W
+// as the page writes it), all bf16. The product is computed transposed:
+// O^T tile (128 output features x NB batch rows) = W^T tile x (X ⊙ G)^T, so
+// the W tile is the 128-row A operand (MN-major straight from W's layout) and
+// the batch is the MMA's N (16..256). That keeps the tensor core's M at 128
+// for any batch, and W -- the large operand -- is streamed once.
+//
+// CTA roles (384 threads):
+//   warp 0      TMA: per 64-wide K step, W (two 64 x 64 boxes) and X (64 x NB)
+//               into a ring of `stages` slots, 128-byte swizzle
+//   warp 1      TMEM allocation; tcgen05.mma issue (one elected lane)
+//   warps 4-11  per K step: X -> X ⊙ G in place (bf16) and the repaired
+//               sum of squares of X; after the loop, the epilogue
+// Grid: (output-feature tiles of 128, batch tiles of NB, splits); the
+// `splits` CTAs that share an output tile form one thread-block cluster and
+// each reduces a contiguous range of K steps. Their fp32 partial tiles and
+// (E, s) pairs go to shared memory, and after a cluster barrier each CTA sums
+// one slice of output features over the cluster through distributed shared
+// memory, scales it and stores bf16. A cluster of one needs no exchange.
+#include "common.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr int kRmThreads = 384;
+constexpr int kCvtWarp0 = 4;                  // warps 4..11 convert and finish
+constexpr int kCvtWarps = 8;
+constexpr uint32_t kWBox = 64 * 128;          // 64 K rows x 64 features (128 B)
+constexpr uint32_t kWStageBytes = 2 * kWBox;  // 128 features
+constexpr int kEmptyExp = -1000;              // row exponent before any nonzero value
+constexpr int kMinExp = -100;                 // references below 2^-100 are raised to it
+
+struct RmsSmem {
+    uint64_t full[kRmsMaxStages];     // TMA bytes landed
+    uint64_t xready[kRmsMaxStages];   // X ⊙ G written (one arrive per converter warp)
+    uint64_t empty[kRmsMaxStages];    // MMAs that read the slot completed
+    uint64_t acc_full;                // every MMA of this CTA completed
+    uint32_t tmem_base;
+    int abort;
+    alignas(128) uint16_t gbuf[kRmsMaxStages][64];   // G chunk of each ring slot
+    int part_e[256];                  // per converter group: partial (E, s) per batch row
+    float part_s[256];
+    int row_e[256];                   // this CTA's partial (E, s) per batch row
+    float row_s[256];
+    float row_p[256];                 // 2^-E of the merged row
+    float row_c[256];                 // 1 / sqrt(s / H + eps 2^-2E) of the merged row
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of all CTAs of the cluster; release/acquire orders the shared
+// memory writes before it with the distributed reads after it.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+
+// Untiled bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Barrier over the converter warps only (named barrier 1).
+__device__ __forceinline__ void converter_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kCvtWarps * 32) : "memory");
+}
+
+// Largest |x| of 8 bf16 values, as the bit pattern of a non-negative bf16
+// (non-negative bf16 patterns order like their values).
+__device__ __forceinline__ uint32_t max_abs_bits8(const uint4& v) {
+    const uint32_t w[4] = {v.x & 0x7fff7fffu, v.y & 0x7fff7fffu, v.z & 0x7fff7fffu,
+                           v.w & 0x7fff7fffu};
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0xffffu, w[i] >> 16));
+    return m;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                               *reinterpret_cast<const __nv_bfloat162*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Per 16-bit half: max(|a|, |b|) (the sign bit is the XOR of the inputs' and
+// is cleared by the caller).
+__device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// sum of (x * sc)^2 over the two bf16 values of a word
+__device__ __forceinline__ float sq2(uint32_t w, float sc, float acc) {
+    const float lo = __uint_as_float(w << 16) * sc;
+    const float hi = __uint_as_float(w & 0xffff0000u) * sc;
+    return fmaf(hi, hi, fmaf(lo, lo, acc));
+}
+
+}  // namespace
+
+// A converter group of cvt_warps = ceil(NB / 32) warps handles one K step
+// (one thread per batch row); cvt_groups groups take the K steps in turn, so
+// several steps are converted at once.
+__global__ void __launch_bounds__(kRmThreads, 2)
+    rmsnorm_matmul_kernel(const __grid_constant__ CUtensorMap tmX,
+                          const __grid_constant__ CUtensorMap tmW, RmsParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ RmsSmem sm;
+    uint8_t* ring = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int NB = p.NB;
+    const int NS = p.stages;
+    const uint32_t xbytes = uint32_t(NB) * 128u;
+    const uint32_t stage_bytes = kWStageBytes + xbytes;
+    const int n0 = blockIdx.x * 128;
+    const int b0 = blockIdx.y * NB;
+    const uint32_t rank = cluster_rank();
+    const int S = p.splits;
+    const int kt0 = int((long long)rank * p.k_tiles / S);
+    const int kt1 = int((long long)(rank + 1) * p.k_tiles / S);
+    const int nk = kt1 - kt0;
+    uint32_t ncols = 32;
+    while (ncols < uint32_t(NB)) ncols <<= 1;
+
+    int issued = 0;   // K steps whose loads were issued (producer thread)
+    auto issue = [&](int i) {
+        const int s = i % NS;
+        uint8_t* st = ring + size_t(s) * stage_bytes;
+        const int k = (kt0 + i) * 64;
+        const uint32_t gbytes = uint32_t(min(64, p.H - k)) * 2u;
+        mbar_arrive_expect_tx(&sm.full[s], stage_bytes + gbytes);
+        bulk_load(sm.gbuf[s], p.G + k, gbytes, &sm.full[s]);
+        tma_load_3d(st, &tmW, &sm.full[s], n0, k, 0);
+        tma_load_3d(st + kWBox, &tmW, &sm.full[s], n0 + 64, k, 0);
+        tma_load_3d(st + kWStageBytes, &tmX, &sm.full[s], k, b0, 0);
+        issued = i + 1;
+    };
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.xready[i], p.cvt_warps);
+            mbar_init(&sm.empty[i], 1);
+        }
+        mbar_init(&sm.acc_full, 1);
+        sm.abort = 0;
+        fence_mbar_init();
+    }
+    // the first ring fill goes out while TMEM is being allocated, one slot
+    // per lane of warp 0
+    if (warp == 0) {
+        __syncwarp();
+        if (lane < min(NS, nk)) issue(lane);
+        issued = min(NS, nk);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&sm.tmem_base, ncols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tacc = sm.tmem_base;
+    volatile int* abort = &sm.abort;
+
+    if (warp == 0) {
+        // ================================================= TMA producer
+        if (lane == 0) {
+            for (int i = NS; i < nk; ++i) {
+                const int st = i % NS;
+                if (!mbar_wait(&sm.empty[st], ((i / NS) - 1) & 1, abort, p.status)) break;
+                issue(i);
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================= MMA issuer
+        const uint32_t idesc = tc::idesc_bf16_ab(128, NB, 1, 0);
+        const uint64_t a0 = tc::sdesc_sw128(smem_u32(ring), kWBox, 1024);
+        const uint64_t b0d = tc::sdesc_sw128(smem_u32(ring + kWStageBytes), 16, 1024);
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % NS;
+            if (!mbar_wait(&sm.xready[s], (i / NS) & 1, abort, p.status)) break;
+            tc::fence_after_sync();
+            const uint64_t so = uint64_t((uint32_t(s) * stage_bytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                tc::mma_bf16_ss_warp(tacc, a0 + so + uint64_t(kk * (2048 >> 4)),
+                                     b0d + so + uint64_t(kk * (32 >> 4)), idesc,
+                                     (i | kk) != 0 ? 1u : 0u);
+            tc::commit_warp(&sm.empty[s]);
+        }
+        // covers every MMA issued above (and arrives at once if none was)
+        tc::commit_warp(&sm.acc_full);
+    } else if (warp >= kCvtWarp0) {
+        // ================================== X ⊙ G and the sum of squares
+        // One thread per batch row of the tile: the row's eight 16-byte chunks
+        // sit in one 128-byte swizzled row, and eight consecutive rows put a
+        // given chunk in eight different bank groups, so the loads are
+        // conflict-free and the row reductions need no shuffles.
+        // Group q converts the K steps of ring slots s with s % ngroups == q
+        // (ngroups divides the ring depth), so each slot has one owner that
+        // waits on the slot's phases in order: a parity wait is only
+        // unambiguous one phase ahead of the barrier.
+        const int cw = warp - kCvtWarp0;                // 0..7
+        const int gw = p.cvt_warps;                     // warps per group
+        const int ngroups = p.cvt_groups;
+        const int grp = cw / gw;
+        const int r = (cw % gw) * 32 + lane;            // batch row of the tile
+        if (grp < ngroups) {
+            int E = kEmptyExp;      // reference exponent: |x| < 2^E for every x seen
+            float Ssum = 0.f;       // sum of (x 2^-E)^2
+            float SC2 = 0.f;        // 2^-2E, set whenever E changes
+            for (int i = grp; i < nk; i += ngroups) {
+                const int s = i % NS;
+                if (!mbar_wait(&sm.full[s], (i / NS) & 1, abort, p.status)) break;
+                if (r < NB) {
+                    uint8_t* row = ring + size_t(s) * stage_bytes + kWStageBytes + r * 128;
+                    const uint32_t sw = uint32_t(r) & 7u;
+                    uint4 v[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        v[j] = *reinterpret_cast<const uint4*>(row + ((uint32_t(j) ^ sw) << 4));
+                    // largest |x| of the row's 64 values (chunk j holds k = 8j .. 8j + 7)
+                    uint32_t m4[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        m4[j] = bf16x2_maxabs(bf16x2_maxabs(v[j].x, v[j].y),
+                                              bf16x2_maxabs(v[j].z, v[j].w));
+                    uint32_t mm = bf16x2_maxabs(
+                        bf16x2_maxabs(bf16x2_maxabs(m4[0], m4[1]), bf16x2_maxabs(m4[2], m4[3])),
+                        bf16x2_maxabs(bf16x2_maxabs(m4[4], m4[5]), bf16x2_maxabs(m4[6], m4[7])));
+                    mm &= 0x7fff7fffu;
+                    const uint32_t mb = max(mm & 0xffffu, mm >> 16);
+                    if (mb != 0u) {
+                        // |x| < 2^(e_biased - 126) for every x of the tile row
+                        const int et = max(int(mb >> 7) - 126, kMinExp);
+                        if (et > E) {
+                            Ssum = ldexpf(Ssum, 2 * (E - et));   // the repair
+                            E = et;
+                            SC2 = ldexpf(1.f, -2 * E);
+                        }
+                        if (et >= -60 && et <= 60) {
+                            // squares of the tile neither overflow nor lose
+                            // anything that matters: sum them unscaled, then
+                            // rescale the tile's sum once
+                            uint64_t a0 = 0, a1 = 0;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                                for (int h = 0; h < 4; h += 2) {
+                                    const uint64_t p0 = f2_pack(__uint_as_float(w[h] << 16),
+                                                                __uint_as_float(w[h] & 0xffff0000u));
+                                    const uint64_t p1 =
+                                        f2_pack(__uint_as_float(w[h + 1] << 16),
+                                                __uint_as_float(w[h + 1] & 0xffff0000u));
+                                    a0 = f2_fma(p0, p0, a0);
+                                    a1 = f2_fma(p1, p1, a1);
+                                }
+                            }
+                            float x0, x1, y0, y1;
+                            f2_unpack(a0, x0, x1);
+                            f2_unpack(a1, y0, y1);
+                            Ssum = fmaf((x0 + x1) + (y0 + y1), SC2, Ssum);
+                        } else {
+                            const float sc = ldexpf(1.f, -E);
+                            float a = Ssum;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                a = sq2(v[j].x, sc, a);
+                                a = sq2(v[j].y, sc, a);
+                                a = sq2(v[j].z, sc, a);
+                                a = sq2(v[j].w, sc, a);
+                            }
+                            Ssum = a;
+                        }
+                    }
+                    // X ⊙ G in place
+                    const uint4* gv = reinterpret_cast<const uint4*>(sm.gbuf[s]);
+                    const bool gfull = (kt0 + i) * 64 + 64 <= p.H;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint4 g = make_uint4(0u, 0u, 0u, 0u);
+                        if (gfull || (kt0 + i) * 64 + j * 8 < p.H) g = gv[j];
+                        uint4 x = v[j];
+                        x.x = bf16x2_mul(x.x, g.x);
+                        x.y = bf16x2_mul(x.y, g.y);
+                        x.z = bf16x2_mul(x.z, g.z);
+                        x.w = bf16x2_mul(x.w, g.w);
+                        *reinterpret_cast<uint4*>(row + ((uint32_t(j) ^ sw) << 4)) = x;
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.xready[s]);
+            }
+            if (r < NB) {
+                sm.part_e[grp * NB + r] = E;
+                sm.part_s[grp * NB + r] = Ssum;
+            }
+        }
+        converter_sync();
+        // merge the groups (the split form of the repair, inside the CTA)
+        for (int r = cw * 32 + lane; r < NB; r += kCvtWarps * 32) {
+            int em = kEmptyExp;
+            for (int q = 0; q < ngroups; ++q) em = max(em, sm.part_e[q * NB + r]);
+            float ss = 0.f;
+            for (int q = 0; q < ngroups; ++q)
+                ss += ldexpf(sm.part_s[q * NB + r], 2 * (sm.part_e[q * NB + r] - em));
+            sm.row_e[r] = em;
+            sm.row_s[r] = ss;
+        }
+
+        // ------------------------------------ accumulator -> shared memory
+        // (the ring is free once every MMA has completed)
+        const bool ok = mbar_wait(&sm.acc_full, 0, abort, p.status);
+        tc::fence_after_sync();
+        if (ok) {
+            const int q4 = warp & 3;                          // TMEM lanes 32 q4 ..
+            const int half = (warp - kCvtWarp0) >> 2;         // column half
+            const int n = q4 * 32 + lane;                     // output feature in the tile
+            float* red = reinterpret_cast<float*>(ring);      // [NB][128]
+            const int c0 = half * (NB / 2);
+            for (int cc = 0; cc < NB / 2; cc += 8) {
+                uint32_t v[8];
+                tc::tmem_ld_32x32b_x8(tacc + (uint32_t(q4 * 32) << 16) + uint32_t(c0 + cc), v);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) red[(c0 + cc + j) * 128 + n] = __uint_as_float(v[j]);
+            }
+        }
+        tc::fence_before_sync();
+    }
+
+    __syncwarp();
+    cluster_sync_all();   // partial tiles and (E, s) of every CTA of the cluster are visible
+
+    // ---- merge the per-row statistics of the cluster (every CTA does it)
+    const uint32_t e_addr = smem_u32(sm.row_e);
+    const uint32_t s_addr = smem_u32(sm.row_s);
+    for (int r = threadIdx.x; r < NB; r += kRmThreads) {
+        int er[8];
+        float sr[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {      // all loads in flight before any use
+            if (q < S) {
+                er[q] = ld_cluster_s32(map_rank(e_addr + 4u * r, q));
+                sr[q] = ld_cluster_f32(map_rank(s_addr + 4u * r, q));
+            }
+        }
+        int em = kEmptyExp;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (q < S) em = max(em, er[q]);
+        float ss = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (q < S) ss += ldexpf(sr[q], 2 * (er[q] - em));   // the repair
+        // O = (acc 2^-E) / sqrt(s / H + eps 2^-2E); fp32 unless E is extreme
+        float pf = 0.f, cf = 0.f;
+        float rms = sqrtf(p.eps);
+        if (ss > 0.f) {
+            const float t = ss / float(p.H);
+            pf = ldexpf(1.f, -em);
+            if (em >= -40 && em <= 40) {
+                cf = rsqrtf(t + ldexpf(p.eps, -2 * em));
+                rms = sqrtf(ldexpf(t, 2 * em) + p.eps);
+            } else {
+                const double td = double(t);
+                cf = float(1.0 / sqrt(td + ldexp(double(p.eps), -2 * em)));
+                rms = float(sqrt(ldexp(td, 2 * em) + double(p.eps)));
+            }
+        }
+        sm.row_p[r] = pf;
+        sm.row_c[r] = cf;
+        if (p.rms && blockIdx.x == 0 && rank == 0 && b0 + r < p.B) p.rms[b0 + r] = rms;
+    }
+    __syncthreads();
+
+    // ---- this CTA's slice of output features, summed over the cluster
+    {
+        const int wd = 128 / S;                 // features per slice
+        const int q4n = wd / 4;
+        const int nlo = int(rank) * wd;
+        const uint32_t red_addr = smem_u32(ring);
+        for (int u = threadIdx.x; u < NB * q4n; u += kRmThreads) {
+            const int r = u / q4n;
+            const int n = nlo + (u % q4n) * 4;
+            const uint32_t a = red_addr + uint32_t(r * 128 + n) * 4u;
+            float4 v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)        // all loads in flight before any use
+                if (q < S) v[q] = ld_cluster_f4(map_rank(a, q));
+            float4 acc = v[0];
+#pragma unroll
+            for (int q = 1; q < 8; ++q) {
+                if (q < S) {
+                    acc.x += v[q].x;
+                    acc.y += v[q].y;
+                    acc.z += v[q].z;
+                    acc.w += v[q].w;
+                }
+            }
+            const int gb = b0 + r, gn = n0 + n;
+            if (gb < p.B && gn < p.D && !*abort) {
+                const float pf = sm.row_p[r], cf = sm.row_c[r];
+                uint2 w;
+                w.x = pack_bf16(acc.x * pf * cf, acc.y * pf * cf);
+                w.y = pack_bf16(acc.z * pf * cf, acc.w * pf * cf);
+                *reinterpret_cast<uint2*>(p.O + size_t(gb) * p.D + gn) = w;
+            }
+        }
+    }
+
+    cluster_sync_all();   // no CTA leaves while another still reads its shared memory
+
+    if (warp == 0 && lane == 0 && *abort) {
+        // let this CTA's copies in flight land before its shared memory is released
+        volatile int never = 0;
+        for (int s = 0; s < NS; ++s) {
+            int last = -1;
+            for (int u = s; u < issued; u += NS) last = u;
+            if (last >= 0) mbar_wait(&sm.full[s], (last / NS) & 1, &never, p.status);
+        }
+    }
+    if (warp == 1) {
+        volatile int never = 0;
+        mbar_wait(&sm.acc_full, 0, &never, p.status);
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tacc, ncols);
+    }
+}
+
+namespace {
+
+constexpr int kMaxDev = 64;
+
+size_t smem_bytes(int NB, int stages) {
+    return size_t(stages) * (kWStageBytes + size_t(NB) * 128u) + 1024;
+}
+
+// Raises the kernel's dynamic shared-memory limit on the current device to at
+// least `smem` (never lowers it).
+bool ensure_smem_attr(int dev, size_t smem) {
+    static size_t attr_set[kMaxDev] = {0};
+    if (attr_set[dev] >= smem) return true;
+    if (cudaFuncSetAttribute(rmsnorm_matmul_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+        return false;
+    attr_set[dev] = smem;
+    return true;
+}
+
+int blocks_per_sm_t(int dev, size_t smem) {
+    int n = 0;
+    if (!ensure_smem_attr(dev, smem) ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rmsnorm_matmul_kernel, kRmThreads,
+                                                      smem) != cudaSuccess ||
+        n < 1) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    return n;
+}
+
+int launch_t(const RmsLaunch& L, int dev, cudaStream_t stream) {
+    const RmsParams& p = L.p;
+    const size_t smem = smem_bytes(p.NB, p.stages);
+    if (!ensure_smem_attr(dev, smem)) return ATTN_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned((p.D + 127) / 128), unsigned((p.B + p.NB - 1) / p.NB),
+                       unsigned(p.splits));
+    cfg.blockDim = dim3(kRmThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = unsigned(p.splits);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, rmsnorm_matmul_kernel, L.tmX, L.tmW, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
+}
+
+}  // namespace
+
+int rmsnorm_matmul_blocks_per_sm(int NB, int stages) {
+    static int cache[kMaxDev][17][kRmsMaxStages + 1] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 1;
+    if (NB < 16 || NB > 256 || NB % 16 || stages < 1 || stages > kRmsMaxStages) return 1;
+    int& c = cache[dev][NB / 16][stages];
+    if (!c) c = blocks_per_sm_t(dev, smem_bytes(NB, stages));
+    return c;
+}
+
+int launch_rmsnorm_matmul(const RmsLaunch& L, cudaStream_t stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return ATTN_ERR_CUDA;
+    return launch_t(L, dev, stream);
+}
+
+}  // namespace attn

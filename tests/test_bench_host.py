@@ -119,3 +119,11 @@ def test_clock_summary_keeps_only_samples_inside_the_region():
 def test_backward_flops_are_two_and_a_half_forward():
     assert bench.backward_flops(2, 3, 100, 130, 64, True) * 2 == \
         5 * bench.prefill_flops(2, 3, 100, 130, 64, True)
+
+
+def test_rmsnorm_matmul_traffic_is_the_weight_at_small_batch():
+    """Mirage §3.3: at small batch the fused kernel is bound by reading the
+    32 MB weight of the LLaMA-2-7B shape (H = D = 4096, bf16)."""
+    b = bench.rmsnorm_matmul_bytes(1, 4096, 4096)
+    assert 32 * 2 ** 20 <= b <= 32 * 2 ** 20 + 64 * 1024
+    assert bench.rmsnorm_matmul_flops(256, 4096, 4096) == 2 * 256 * 4096 * 4096

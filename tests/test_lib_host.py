@@ -143,3 +143,27 @@ def test_backward_validation_before_launch(L):
     assert bwd(wsb=16) == 4
     assert bwd(dK=MIS) == 7
     assert L.attn_backward_workspace_bytes(2, 4, 100, 128) == 2 * 4 * 100 * 129 * 4
+
+
+def test_rmsnorm_matmul_validation_before_launch(L):
+    def rm(X=P, G=P, W=P, O=P, rms=None, B=4, H=256, D=128, eps=0.0, splits=0):
+        return L.attn_rmsnorm_matmul(X, G, W, O, rms, B, H, D, eps, splits, None)
+    assert rm(X=None) == 1
+    assert rm(W=None) == 1
+    assert rm(B=0) == 2
+    assert rm(D=-8) == 2
+    assert rm(H=100) == 3           # not a multiple of 8
+    assert rm(D=12) == 3
+    assert rm(eps=-1.0) == 8
+    assert rm(eps=float("nan")) == 8
+    assert rm(splits=3) == 8
+    assert rm(splits=8, H=256) == 8  # only 4 K steps of 64
+    assert rm(O=MIS) == 7
+    assert rm(rms=ctypes.c_void_p(4098)) == 7
+    def rmt(tile, splits=0):
+        return L.attn_rmsnorm_matmul_tiled(P, P, P, P, None, 4, 256, 128, 0.0, tile, splits, None)
+    assert rmt(24) == 8 and rmt(-16) == 8 and rmt(272) == 8
+    assert L.attn_rmsnorm_matmul_splits(0, 64, 64) < 0
+    S = L.attn_rmsnorm_matmul_splits(16, 4096, 4096)
+    assert S in (1, 2, 4, 8)
+    assert L.attn_rmsnorm_matmul_splits(1, 64, 8) == 1   # one K step
