@@ -93,39 +93,58 @@ int check_common(int B, int Hq, int Hkv, int d, float scale) {
 
 int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
 
-// Tile geometry of the fused RMSNorm + product: batch rows per CTA (one tile
-// when B <= 256, else equal tiles of at most 256), ring depth (about 100 KB so
-// two CTAs can share an SM when the batch tile is small) and the K split:
-// the largest power of two <= 8 that keeps every CTA resident at once and
-// gives each at least one 64-wide K step.
+// Tile geometry of the fused RMSNorm + product.
+//  * batch rows per CTA: one tile when B <= 256 (or the caller's tile), else
+//    equal tiles of at most 256;
+//  * K split: the largest power of two <= 8 that keeps the whole grid
+//    resident (one CTA per SM; two for batch tiles <= 32) and gives each CTA
+//    at least one 64-wide K step;
+//  * shared memory: ~200 KB per CTA when the grid is one CTA per SM, else
+//    ~100 KB (two per SM), less the epilogue's receive area when that gets
+//    its own space (small batch tiles; larger ones reuse the rings); the X
+//    ring takes a third (half for batch tiles >= 128) in 2..8 slots, a
+//    multiple of the converter groups, the W ring the rest (2..12 slots).
 struct RmsGeometry {
-    int NB, stages, splits, k_tiles, cvt_warps, cvt_groups;
+    int NB, w_stages, x_stages, splits, k_tiles, cvt_warps, cvt_groups, recv_separate;
 };
 
-RmsGeometry rms_geometry(int B, int H, int D, int splits_req, int tile_req, bool query_device) {
+RmsGeometry rms_geometry(int B, int H, int D, int splits_req, int tile_req) {
     RmsGeometry g;
     const int tile_max = tile_req > 0 ? tile_req : 256;
     const int b_tiles = ceil_div(B, tile_max);
     g.NB = ceil_div(ceil_div(B, b_tiles), 16) * 16;
-    const int stage_bytes = 16384 + g.NB * 128;
-    g.stages = std::max(3, std::min(kRmsMaxStages, 102400 / stage_bytes));
-    // converter warps per K step: one thread per batch row; the groups that
-    // fit in the 8 converter warps own ring slots in turn, so the ring depth
-    // is rounded down to a multiple of their count
-    g.cvt_warps = ceil_div(g.NB, 32);
-    g.cvt_groups = std::min(8 / g.cvt_warps, g.stages);
-    g.stages = std::max(g.cvt_groups, g.stages / g.cvt_groups * g.cvt_groups);
     g.k_tiles = ceil_div(H, 64);
+    const long long base = (long long)ceil_div(D, 128) * ceil_div(B, g.NB);
+    const long long sms = sm_count();
+    // small batch tiles run two CTAs per SM (their rings fit in ~100 KB)
+    const long long slots = g.NB <= 32 ? 2 * sms : sms;
     if (splits_req > 0) {
         g.splits = splits_req;
-        return g;
+    } else {
+        g.splits = 1;
+        while (g.splits * 2 <= 8 && g.splits * 2 <= g.k_tiles && base * g.splits * 2 <= slots)
+            g.splits *= 2;
     }
-    const long long base = (long long)ceil_div(D, 128) * ceil_div(B, g.NB);
-    const long long slots =
-        (long long)sm_count() * (query_device ? rmsnorm_matmul_blocks_per_sm(g.NB, g.stages) : 1);
-    g.splits = 1;
-    while (g.splits * 2 <= 8 && g.splits * 2 <= g.k_tiles && base * g.splits * 2 <= slots)
-        g.splits *= 2;
+    const int xslot = g.NB * 128;
+    const int wslot = 16384;
+    int budget = base * g.splits <= sms ? 200 * 1024 : 100 * 1024;
+    // the epilogue's receive area: fp32 tile + (E, s) per row and split; it
+    // gets its own space when small, else it reuses the rings
+    const int recv = g.NB * 512 + 8 * g.splits * g.NB;
+    g.recv_separate = recv <= 32 * 1024 + 8 * 8 * 64 ? 1 : 0;
+    if (g.recv_separate) budget -= recv;
+    budget = std::max(budget, recv + wslot);
+    // converter warps per K step: one thread per batch row; the X ring gets a
+    // third of the space (half for large batch tiles, whose X slots are big)
+    g.cvt_warps = ceil_div(g.NB, 32);
+    const int x_share = g.NB >= 128 ? budget / 2 : budget / 3;
+    g.x_stages = std::max(2, std::min(kRmsMaxXStages, x_share / xslot));
+    g.cvt_groups = std::min(8 / g.cvt_warps, g.x_stages);
+    g.x_stages = std::max(g.cvt_groups, g.x_stages / g.cvt_groups * g.cvt_groups);
+    g.w_stages = std::max(2, std::min(kRmsMaxWStages, (budget - g.x_stages * xslot) / wslot));
+    while (!g.recv_separate && g.w_stages < kRmsMaxWStages &&
+           g.w_stages * wslot + g.x_stages * xslot < recv)
+        ++g.w_stages;
     return g;
 }
 
@@ -322,9 +341,7 @@ int attn_backward(const void* Q, const void* K, const void* V, const void* O, co
 
 int attn_rmsnorm_matmul_splits(int B, int H, int D) {
     if (B <= 0 || H <= 0 || D <= 0) return -ATTN_ERR_SHAPE;
-    int dev = 0;
-    const bool have_dev = cudaGetDevice(&dev) == cudaSuccess;
-    return rms_geometry(B, H, D, 0, 0, have_dev).splits;
+    return rms_geometry(B, H, D, 0, 0).splits;
 }
 
 int attn_rmsnorm_matmul(const void* X, const void* G, const void* W, void* O, float* rms, int B,
@@ -348,7 +365,7 @@ int attn_rmsnorm_matmul_tiled(const void* X, const void* G, const void* W, void*
     for (const void* p : ptrs)
         if (!aligned16(p)) return ATTN_ERR_ALIGN;
     if (rms && (reinterpret_cast<uintptr_t>(rms) & 3u)) return ATTN_ERR_ALIGN;
-    const RmsGeometry g = rms_geometry(B, H, D, splits, batch_tile, true);
+    const RmsGeometry g = rms_geometry(B, H, D, splits, batch_tile);
     RmsLaunch L;
     std::memset(&L, 0, sizeof(L));
     L.p.O = static_cast<__nv_bfloat16*>(O);
@@ -360,9 +377,11 @@ int attn_rmsnorm_matmul_tiled(const void* X, const void* G, const void* W, void*
     L.p.NB = g.NB;
     L.p.splits = g.splits;
     L.p.k_tiles = g.k_tiles;
-    L.p.stages = g.stages;
+    L.p.w_stages = g.w_stages;
+    L.p.x_stages = g.x_stages;
     L.p.cvt_warps = g.cvt_warps;
     L.p.cvt_groups = g.cvt_groups;
+    L.p.recv_separate = g.recv_separate;
     L.p.eps = eps;
     L.p.status = status_ptr();
     int st;

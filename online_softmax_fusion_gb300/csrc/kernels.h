@@ -90,9 +90,11 @@ struct RmsParams {
     int NB;                                   // batch rows per CTA (multiple of 16, <= 256)
     int splits;                               // CTAs of a cluster sharing one output tile (K split)
     int k_tiles;                              // ceil(H / 64)
-    int stages;                               // ring depth
+    int w_stages;                             // W ring depth
+    int x_stages;                             // X ring depth
     int cvt_warps;                            // converter warps per K step (<= 8)
-    int cvt_groups;                           // groups taking K steps in turn; divides stages
+    int cvt_groups;                           // groups taking K steps in turn; divides x_stages
+    int recv_separate;                        // the epilogue's receive area follows the rings
     float eps;
     int* status;
 };
@@ -102,8 +104,8 @@ struct RmsLaunch {
     RmsParams p;
 };
 
-constexpr int kRmsMaxStages = 8;
+constexpr int kRmsMaxWStages = 12;
+constexpr int kRmsMaxXStages = 8;
 int launch_rmsnorm_matmul(const RmsLaunch& L, cudaStream_t stream);
-int rmsnorm_matmul_blocks_per_sm(int NB, int stages);   // 1 when no device answers
 
 }  // namespace attn

@@ -23,18 +23,25 @@
 // the batch is the MMA's N (16..256). That keeps the tensor core's M at 128
 // for any batch, and W -- the large operand -- is streamed once.
 //
-// CTA roles (384 threads):
-//   warp 0      TMA: per 64-wide K step, W (two 64 x 64 boxes) and X (64 x NB)
-//               into a ring of `stages` slots, 128-byte swizzle
+// CTA roles (384 threads), two rings with their own depths:
+//   warp 0      TMA of W: per 64-wide K step two 64 x 64 boxes (128-byte
+//               swizzle) into the W ring
+//   warp 2      TMA of X (64 x NB box) and a bulk copy of G's 64 entries into
+//               the X ring
 //   warp 1      TMEM allocation; tcgen05.mma issue (one elected lane)
 //   warps 4-11  per K step: X -> X ⊙ G in place (bf16) and the repaired
 //               sum of squares of X; after the loop, the epilogue
+// W needs no conversion, so a W slot's round trip is load -> MMA -> free,
+// and the W ring is deep; X slots are converted ahead of the MMA.
 // Grid: (output-feature tiles of 128, batch tiles of NB, splits); the
 // `splits` CTAs that share an output tile form one thread-block cluster and
-// each reduces a contiguous range of K steps. Their fp32 partial tiles and
-// (E, s) pairs go to shared memory, and after a cluster barrier each CTA sums
-// one slice of output features over the cluster through distributed shared
-// memory, scales it and stores bf16. A cluster of one needs no exchange.
+// each reduces a contiguous range of K steps. Each CTA then pushes its fp32
+// partial tile, slice by slice, and its (E, s) pairs into the other CTAs'
+// shared memory (distributed shared memory stores); after one cluster
+// barrier each CTA sums its slice of output features from its own shared
+// memory, scales it and stores bf16.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
@@ -52,13 +59,15 @@ constexpr int kEmptyExp = -1000;              // row exponent before any nonzero
 constexpr int kMinExp = -100;                 // references below 2^-100 are raised to it
 
 struct RmsSmem {
-    uint64_t full[kRmsMaxStages];     // TMA bytes landed
-    uint64_t xready[kRmsMaxStages];   // X ⊙ G written (one arrive per converter warp)
-    uint64_t empty[kRmsMaxStages];    // MMAs that read the slot completed
+    uint64_t wfull[kRmsMaxWStages];   // W tile landed
+    uint64_t wempty[kRmsMaxWStages];  // MMAs that read the W slot completed
+    uint64_t xfull[kRmsMaxXStages];   // X tile and G chunk landed
+    uint64_t xready[kRmsMaxXStages];  // X ⊙ G written (one arrive per converter warp)
+    uint64_t xempty[kRmsMaxXStages];  // MMAs that read the X slot completed
     uint64_t acc_full;                // every MMA of this CTA completed
     uint32_t tmem_base;
     int abort;
-    alignas(128) uint16_t gbuf[kRmsMaxStages][64];   // G chunk of each ring slot
+    alignas(128) uint16_t gbuf[kRmsMaxXStages][64];  // G chunk of each X slot
     int part_e[256];                  // per converter group: partial (E, s) per batch row
     float part_s[256];
     int row_e[256];                   // this CTA's partial (E, s) per batch row
@@ -87,25 +96,8 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t a) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(a)
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
-    int v;
-    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-    return v;
+__device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
 // Untiled bulk copy global -> shared (16-byte aligned, size a multiple of 16),
@@ -172,9 +164,11 @@ __global__ void __launch_bounds__(kRmThreads, 2)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int NB = p.NB;
-    const int NS = p.stages;
+    const int NW = p.w_stages;
+    const int NX = p.x_stages;
     const uint32_t xbytes = uint32_t(NB) * 128u;
-    const uint32_t stage_bytes = kWStageBytes + xbytes;
+    uint8_t* wring = ring;
+    uint8_t* xring = ring + size_t(NW) * kWStageBytes;
     const int n0 = blockIdx.x * 128;
     const int b0 = blockIdx.y * NB;
     const uint32_t rank = cluster_rank();
@@ -185,37 +179,45 @@ __global__ void __launch_bounds__(kRmThreads, 2)
     uint32_t ncols = 32;
     while (ncols < uint32_t(NB)) ncols <<= 1;
 
-    int issued = 0;   // K steps whose loads were issued (producer thread)
-    auto issue = [&](int i) {
-        const int s = i % NS;
-        uint8_t* st = ring + size_t(s) * stage_bytes;
+    auto issue_w = [&](int i) {
+        const int s = i % NW;
+        uint8_t* st = wring + size_t(s) * kWStageBytes;
+        const int k = (kt0 + i) * 64;
+        mbar_arrive_expect_tx(&sm.wfull[s], kWStageBytes);
+        tma_load_3d(st, &tmW, &sm.wfull[s], n0, k, 0);
+        tma_load_3d(st + kWBox, &tmW, &sm.wfull[s], n0 + 64, k, 0);
+    };
+    auto issue_x = [&](int i) {
+        const int s = i % NX;
         const int k = (kt0 + i) * 64;
         const uint32_t gbytes = uint32_t(min(64, p.H - k)) * 2u;
-        mbar_arrive_expect_tx(&sm.full[s], stage_bytes + gbytes);
-        bulk_load(sm.gbuf[s], p.G + k, gbytes, &sm.full[s]);
-        tma_load_3d(st, &tmW, &sm.full[s], n0, k, 0);
-        tma_load_3d(st + kWBox, &tmW, &sm.full[s], n0 + 64, k, 0);
-        tma_load_3d(st + kWStageBytes, &tmX, &sm.full[s], k, b0, 0);
-        issued = i + 1;
+        mbar_arrive_expect_tx(&sm.xfull[s], xbytes + gbytes);
+        bulk_load(sm.gbuf[s], p.G + k, gbytes, &sm.xfull[s]);
+        tma_load_3d(xring + size_t(s) * xbytes, &tmX, &sm.xfull[s], k, b0, 0);
     };
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmX);
         tma_prefetch_desc(&tmW);
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&sm.full[i], 1);
+        for (int i = 0; i < NW; ++i) {
+            mbar_init(&sm.wfull[i], 1);
+            mbar_init(&sm.wempty[i], 1);
+        }
+        for (int i = 0; i < NX; ++i) {
+            mbar_init(&sm.xfull[i], 1);
             mbar_init(&sm.xready[i], p.cvt_warps);
-            mbar_init(&sm.empty[i], 1);
+            mbar_init(&sm.xempty[i], 1);
         }
         mbar_init(&sm.acc_full, 1);
         sm.abort = 0;
         fence_mbar_init();
     }
-    // the first ring fill goes out while TMEM is being allocated, one slot
-    // per lane of warp 0
+    // the first fill of both rings goes out while TMEM is being allocated:
+    // lanes 0.. of warp 0 issue W slots, lanes 16.. issue X slots
+    const int w_first = min(NW, nk), x_first = min(NX, nk);
     if (warp == 0) {
         __syncwarp();
-        if (lane < min(NS, nk)) issue(lane);
-        issued = min(NS, nk);
+        if (lane < w_first) issue_w(lane);
+        if (lane >= 16 && lane - 16 < x_first) issue_x(lane - 16);
     }
     if (warp == 1) {
         tc::tmem_alloc(&sm.tmem_base, ncols);
@@ -227,31 +229,46 @@ __global__ void __launch_bounds__(kRmThreads, 2)
     const uint32_t tacc = sm.tmem_base;
     volatile int* abort = &sm.abort;
 
+    int w_issued = w_first, x_issued = x_first;   // loads issued (producer threads)
     if (warp == 0) {
-        // ================================================= TMA producer
+        // ============================================== TMA producer of W
         if (lane == 0) {
-            for (int i = NS; i < nk; ++i) {
-                const int st = i % NS;
-                if (!mbar_wait(&sm.empty[st], ((i / NS) - 1) & 1, abort, p.status)) break;
-                issue(i);
+            for (int i = NW; i < nk; ++i) {
+                const int st = i % NW;
+                if (!mbar_wait(&sm.wempty[st], ((i / NW) - 1) & 1, abort, p.status)) break;
+                issue_w(i);
+                w_issued = i + 1;
+            }
+        }
+    } else if (warp == 2) {
+        // ======================================== TMA producer of X and G
+        if (lane == 0) {
+            for (int i = NX; i < nk; ++i) {
+                const int st = i % NX;
+                if (!mbar_wait(&sm.xempty[st], ((i / NX) - 1) & 1, abort, p.status)) break;
+                issue_x(i);
+                x_issued = i + 1;
             }
         }
     } else if (warp == 1) {
         // ================================================= MMA issuer
         const uint32_t idesc = tc::idesc_bf16_ab(128, NB, 1, 0);
-        const uint64_t a0 = tc::sdesc_sw128(smem_u32(ring), kWBox, 1024);
-        const uint64_t b0d = tc::sdesc_sw128(smem_u32(ring + kWStageBytes), 16, 1024);
+        const uint64_t a0 = tc::sdesc_sw128(smem_u32(wring), kWBox, 1024);
+        const uint64_t b0d = tc::sdesc_sw128(smem_u32(xring), 16, 1024);
         for (int i = 0; i < nk; ++i) {
-            const int s = i % NS;
-            if (!mbar_wait(&sm.xready[s], (i / NS) & 1, abort, p.status)) break;
+            const int sw = i % NW, sx = i % NX;
+            if (!mbar_wait(&sm.xready[sx], (i / NX) & 1, abort, p.status)) break;
+            if (!mbar_wait(&sm.wfull[sw], (i / NW) & 1, abort, p.status)) break;
             tc::fence_after_sync();
-            const uint64_t so = uint64_t((uint32_t(s) * stage_bytes) >> 4);
+            const uint64_t wo = uint64_t((uint32_t(sw) * kWStageBytes) >> 4);
+            const uint64_t xo = uint64_t((uint32_t(sx) * xbytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                tc::mma_bf16_ss_warp(tacc, a0 + so + uint64_t(kk * (2048 >> 4)),
-                                     b0d + so + uint64_t(kk * (32 >> 4)), idesc,
+                tc::mma_bf16_ss_warp(tacc, a0 + wo + uint64_t(kk * (2048 >> 4)),
+                                     b0d + xo + uint64_t(kk * (32 >> 4)), idesc,
                                      (i | kk) != 0 ? 1u : 0u);
-            tc::commit_warp(&sm.empty[s]);
+            tc::commit_warp(&sm.wempty[sw]);
+            tc::commit_warp(&sm.xempty[sx]);
         }
         // covers every MMA issued above (and arrives at once if none was)
         tc::commit_warp(&sm.acc_full);
@@ -261,8 +278,8 @@ __global__ void __launch_bounds__(kRmThreads, 2)
         // sit in one 128-byte swizzled row, and eight consecutive rows put a
         // given chunk in eight different bank groups, so the loads are
         // conflict-free and the row reductions need no shuffles.
-        // Group q converts the K steps of ring slots s with s % ngroups == q
-        // (ngroups divides the ring depth), so each slot has one owner that
+        // Group q converts the K steps of X slots s with s % ngroups == q
+        // (ngroups divides the X ring depth), so each slot has one owner that
         // waits on the slot's phases in order: a parity wait is only
         // unambiguous one phase ahead of the barrier.
         const int cw = warp - kCvtWarp0;                // 0..7
@@ -275,10 +292,10 @@ __global__ void __launch_bounds__(kRmThreads, 2)
             float Ssum = 0.f;       // sum of (x 2^-E)^2
             float SC2 = 0.f;        // 2^-2E, set whenever E changes
             for (int i = grp; i < nk; i += ngroups) {
-                const int s = i % NS;
-                if (!mbar_wait(&sm.full[s], (i / NS) & 1, abort, p.status)) break;
+                const int s = i % NX;
+                if (!mbar_wait(&sm.xfull[s], (i / NX) & 1, abort, p.status)) break;
                 if (r < NB) {
-                    uint8_t* row = ring + size_t(s) * stage_bytes + kWStageBytes + r * 128;
+                    uint8_t* row = xring + size_t(s) * xbytes + r * 128;
                     const uint32_t sw = uint32_t(r) & 7u;
                     uint4 v[8];
 #pragma unroll
@@ -375,50 +392,64 @@ __global__ void __launch_bounds__(kRmThreads, 2)
             sm.row_s[r] = ss;
         }
 
-        // ------------------------------------ accumulator -> shared memory
-        // (the ring is free once every MMA has completed)
-        const bool ok = mbar_wait(&sm.acc_full, 0, abort, p.status);
-        tc::fence_after_sync();
-        if (ok) {
-            const int q4 = warp & 3;                          // TMEM lanes 32 q4 ..
-            const int half = (warp - kCvtWarp0) >> 2;         // column half
-            const int n = q4 * 32 + lane;                     // output feature in the tile
-            float* red = reinterpret_cast<float*>(ring);      // [NB][128]
-            const int c0 = half * (NB / 2);
-            for (int cc = 0; cc < NB / 2; cc += 8) {
-                uint32_t v[8];
-                tc::tmem_ld_32x32b_x8(tacc + (uint32_t(q4 * 32) << 16) + uint32_t(c0 + cc), v);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) red[(c0 + cc + j) * 128 + n] = __uint_as_float(v[j]);
-            }
-        }
         tc::fence_before_sync();
     }
 
+    // ================================================================ epilogue
+    // Each CTA pushes its fp32 partial tile, split into `S` slices of
+    // 128 / S output features, into the slice owners' shared memory, and its
+    // per-row (E, s) into every CTA's; after one cluster barrier every CTA
+    // merges and reduces from its own shared memory only. The receive area
+    // sits after the rings when it fits there; otherwise it reuses the rings,
+    // and a first cluster barrier makes sure every CTA's rings are idle.
     __syncwarp();
-    cluster_sync_all();   // partial tiles and (E, s) of every CTA of the cluster are visible
-
-    // ---- merge the per-row statistics of the cluster (every CTA does it)
-    const uint32_t e_addr = smem_u32(sm.row_e);
-    const uint32_t s_addr = smem_u32(sm.row_s);
-    for (int r = threadIdx.x; r < NB; r += kRmThreads) {
-        int er[8];
-        float sr[8];
+    bool ok = true;
+    if (warp >= kCvtWarp0) {
+        ok = mbar_wait(&sm.acc_full, 0, abort, p.status);
+        tc::fence_after_sync();
+    }
+    __syncthreads();                          // this CTA's (E, s) rows are in sm.row_e / row_s
+    if (!p.recv_separate) cluster_sync_all();
+    const int wd = 128 / S;                   // output features per slice
+    uint8_t* recv = ring + (p.recv_separate ? size_t(NW) * kWStageBytes + size_t(NX) * xbytes : 0);
+    const uint32_t recv_a = smem_u32(recv);
+    const uint32_t tile_bytes = uint32_t(NB) * 128u * 4u;           // [S][NB][wd] fp32
+    const uint32_t e_off = tile_bytes;                               // [S][NB] int
+    const uint32_t s_off = tile_bytes + uint32_t(S * NB) * 4u;       // [S][NB] fp32
+    if (warp >= kCvtWarp0 && ok) {
+        const int q4 = warp & 3;                          // TMEM lanes 32 q4 ..
+        const int half = (warp - kCvtWarp0) >> 2;         // column half
+        const int n = q4 * 32 + lane;                     // output feature in the tile
+        const int owner = n / wd;
+        const uint32_t dst = map_rank(recv_a, uint32_t(owner)) +
+                             uint32_t((int(rank) * NB * wd + (n - owner * wd)) * 4);
+        const int c0 = half * (NB / 2);
+        for (int cc = 0; cc < NB / 2; cc += 8) {
+            uint32_t v[8];
+            tc::tmem_ld_32x32b_x8(tacc + (uint32_t(q4 * 32) << 16) + uint32_t(c0 + cc), v);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {      // all loads in flight before any use
-            if (q < S) {
-                er[q] = ld_cluster_s32(map_rank(e_addr + 4u * r, q));
-                sr[q] = ld_cluster_f32(map_rank(s_addr + 4u * r, q));
-            }
+            for (int j = 0; j < 8; ++j)
+                st_cluster_u32(dst + uint32_t((c0 + cc + j) * wd * 4), v[j]);
         }
+    }
+    for (int idx = threadIdx.x; idx < S * NB; idx += kRmThreads) {
+        const int q = idx / NB, r = idx - (idx / NB) * NB;
+        const uint32_t o = uint32_t((int(rank) * NB + r) * 4);
+        const uint32_t base = map_rank(recv_a, uint32_t(q));
+        st_cluster_u32(base + e_off + o, uint32_t(sm.row_e[r]));
+        st_cluster_u32(base + s_off + o, __float_as_uint(sm.row_s[r]));
+    }
+    tc::fence_before_sync();
+    cluster_sync_all();   // every push of every CTA of the cluster has landed
+
+    // ---- merge the per-row statistics of the cluster (local)
+    const int* re = reinterpret_cast<const int*>(recv + e_off);
+    const float* rs = reinterpret_cast<const float*>(recv + s_off);
+    for (int r = threadIdx.x; r < NB; r += kRmThreads) {
         int em = kEmptyExp;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            if (q < S) em = max(em, er[q]);
+        for (int q = 0; q < S; ++q) em = max(em, re[q * NB + r]);
         float ss = 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            if (q < S) ss += ldexpf(sr[q], 2 * (er[q] - em));   // the repair
+        for (int q = 0; q < S; ++q) ss += ldexpf(rs[q * NB + r], 2 * (re[q * NB + r] - em));   // the repair
         // O = (acc 2^-E) / sqrt(s / H + eps 2^-2E); fp32 unless E is extreme
         float pf = 0.f, cf = 0.f;
         float rms = sqrtf(p.eps);
@@ -440,31 +471,23 @@ __global__ void __launch_bounds__(kRmThreads, 2)
     }
     __syncthreads();
 
-    // ---- this CTA's slice of output features, summed over the cluster
+    // ---- this CTA's slice of output features, summed over the cluster (local)
     {
-        const int wd = 128 / S;                 // features per slice
         const int q4n = wd / 4;
         const int nlo = int(rank) * wd;
-        const uint32_t red_addr = smem_u32(ring);
+        const float* rt = reinterpret_cast<const float*>(recv);
         for (int u = threadIdx.x; u < NB * q4n; u += kRmThreads) {
             const int r = u / q4n;
-            const int n = nlo + (u % q4n) * 4;
-            const uint32_t a = red_addr + uint32_t(r * 128 + n) * 4u;
-            float4 v[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)        // all loads in flight before any use
-                if (q < S) v[q] = ld_cluster_f4(map_rank(a, q));
-            float4 acc = v[0];
-#pragma unroll
-            for (int q = 1; q < 8; ++q) {
-                if (q < S) {
-                    acc.x += v[q].x;
-                    acc.y += v[q].y;
-                    acc.z += v[q].z;
-                    acc.w += v[q].w;
-                }
+            const int nl = (u - r * q4n) * 4;
+            float4 acc = *reinterpret_cast<const float4*>(rt + r * wd + nl);
+            for (int q = 1; q < S; ++q) {
+                const float4 v = *reinterpret_cast<const float4*>(rt + (q * NB + r) * wd + nl);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
             }
-            const int gb = b0 + r, gn = n0 + n;
+            const int gb = b0 + r, gn = n0 + nlo + nl;
             if (gb < p.B && gn < p.D && !*abort) {
                 const float pf = sm.row_p[r], cf = sm.row_c[r];
                 uint2 w;
@@ -475,15 +498,16 @@ __global__ void __launch_bounds__(kRmThreads, 2)
         }
     }
 
-    cluster_sync_all();   // no CTA leaves while another still reads its shared memory
-
-    if (warp == 0 && lane == 0 && *abort) {
+    if (*abort && lane == 0 && (warp == 0 || warp == 2)) {
         // let this CTA's copies in flight land before its shared memory is released
         volatile int never = 0;
-        for (int s = 0; s < NS; ++s) {
+        const int nst = warp == 0 ? NW : NX;
+        const int iss = warp == 0 ? w_issued : x_issued;
+        uint64_t* full = warp == 0 ? sm.wfull : sm.xfull;
+        for (int s = 0; s < nst; ++s) {
             int last = -1;
-            for (int u = s; u < issued; u += NS) last = u;
-            if (last >= 0) mbar_wait(&sm.full[s], (last / NS) & 1, &never, p.status);
+            for (int u = s; u < iss; u += nst) last = u;
+            if (last >= 0) mbar_wait(&full[s], (last / nst) & 1, &never, p.status);
         }
     }
     if (warp == 1) {
@@ -498,8 +522,10 @@ namespace {
 
 constexpr int kMaxDev = 64;
 
-size_t smem_bytes(int NB, int stages) {
-    return size_t(stages) * (kWStageBytes + size_t(NB) * 128u) + 1024;
+size_t smem_bytes(const RmsParams& p) {
+    const size_t rings = size_t(p.w_stages) * kWStageBytes + size_t(p.x_stages) * size_t(p.NB) * 128u;
+    const size_t recv = size_t(p.NB) * 512u + size_t(8 * p.splits * p.NB);
+    return (p.recv_separate ? rings + recv : std::max(rings, recv)) + 1024;
 }
 
 // Raises the kernel's dynamic shared-memory limit on the current device to at
@@ -514,21 +540,9 @@ bool ensure_smem_attr(int dev, size_t smem) {
     return true;
 }
 
-int blocks_per_sm_t(int dev, size_t smem) {
-    int n = 0;
-    if (!ensure_smem_attr(dev, smem) ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rmsnorm_matmul_kernel, kRmThreads,
-                                                      smem) != cudaSuccess ||
-        n < 1) {
-        (void)cudaGetLastError();
-        return 1;
-    }
-    return n;
-}
-
 int launch_t(const RmsLaunch& L, int dev, cudaStream_t stream) {
     const RmsParams& p = L.p;
-    const size_t smem = smem_bytes(p.NB, p.stages);
+    const size_t smem = smem_bytes(p);
     if (!ensure_smem_attr(dev, smem)) return ATTN_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned((p.D + 127) / 128), unsigned((p.B + p.NB - 1) / p.NB),
@@ -551,16 +565,6 @@ int launch_t(const RmsLaunch& L, int dev, cudaStream_t stream) {
 }
 
 }  // namespace
-
-int rmsnorm_matmul_blocks_per_sm(int NB, int stages) {
-    static int cache[kMaxDev][17][kRmsMaxStages + 1] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 1;
-    if (NB < 16 || NB > 256 || NB % 16 || stages < 1 || stages > kRmsMaxStages) return 1;
-    int& c = cache[dev][NB / 16][stages];
-    if (!c) c = blocks_per_sm_t(dev, smem_bytes(NB, stages));
-    return c;
-}
 
 int launch_rmsnorm_matmul(const RmsLaunch& L, cudaStream_t stream) {
     int dev = 0;
