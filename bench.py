@@ -441,6 +441,40 @@ def run_reference(args):
     return 0
 
 
+# ------------------------------------------------- RMSNorm + MatMul only
+def run_rmsnorm(args):
+    """Times the fused RMSNorm + product alone at the LLaMA-2-7B shape
+    (H = D = 4096) with --batch rows: `warmup` untimed then `steps` timed
+    launches, each reading one of 5 copies of W in turn (5 x 32 MB > L2)."""
+    import torch
+    import online_softmax_fusion_gb300 as attn
+    import workloads as W
+    attn.lib()
+    peaks, _ = load_peaks()
+    cfg = W.RmsMatmulConfig(f"rmsnorm_matmul_llama7b_b{args.batch}", B=args.batch, H=4096,
+                            D=4096, seed=1301)
+    rin = W.make_rmsnorm_matmul_inputs(cfg, "cuda")
+    wcopies = [rin["w"]] + [rin["w"].clone() for _ in range(4)]
+    O = torch.empty((cfg.B, cfg.D), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    it = [0]
+
+    def step():
+        attn.rmsnorm_matmul(rin["x"], rin["g"], wcopies[it[0] % 5], out=O)
+        it[0] += 1
+    ms = time_launches(step, args.steps, args.warmup, stream)
+    byts = rmsnorm_matmul_bytes(cfg.B, cfg.H, cfg.D)
+    fl = rmsnorm_matmul_flops(cfg.B, cfg.H, cfg.D)
+    gbs = byts / (ms * 1e-3) / 1e9
+    print(json.dumps({"metric": "RMSNorm+MatMul GB/s", "value": gbs, "unit": "GB/s",
+                      "workload": cfg.name, "ms_per_launch": ms,
+                      "frac_hbm": gbs / peaks["hbm_gbs"],
+                      "tflops": fl / (ms * 1e-3) / 1e12, "steps": args.steps,
+                      "warmup": args.warmup, "timing": "eager launches, CUDA events"}),
+          flush=True)
+    return 0
+
+
 # -------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -650,8 +684,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip the secondary GQA sweep / long-decode measurements")
-    ap.add_argument("--kernel", choices=["all", "prefill", "decode"], default="all",
-                    help="time the whole step (default) or one form only (profiling)")
+    ap.add_argument("--kernel", choices=["all", "prefill", "decode", "rmsnorm"], default="all",
+                    help="time the whole step (default) or one kernel only (profiling)")
+    ap.add_argument("--batch", type=int, default=16,
+                    help="batch rows of the RMSNorm + MatMul workload (--kernel rmsnorm)")
     ap.add_argument("--small", action="store_true",
                     help="decode on a quarter of the batch (profiling captures)")
     args = ap.parse_args(argv)
@@ -659,6 +695,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.kernel == "rmsnorm":
+        return run_rmsnorm(args)
     return run_ours(args)
 
 
