@@ -151,6 +151,20 @@ int attn_backward(const void* Q, const void* K, const void* V,
                   int causal, float scale, const float* alibi_slopes,
                   void* workspace, size_t workspace_bytes, void* stream);
 
+/* attn_backward with the implementation chosen: ATTN_IMPL_TCGEN05 (head dim
+ * 128 only: one CTA per 128-key block, the five products on tcgen05 with
+ * S^T, dP^T, dQ^T, dV and dK in tensor memory, dQ added to the workspace
+ * accumulator by TMA reduce-add), ATTN_IMPL_MMA_SYNC (register-tile form,
+ * head dims 64 and 128, dQ added with atomics), or ATTN_IMPL_AUTO (tcgen05
+ * for head dim 128, else mma.sync). ATTN_ERR_UNSUPPORTED for any other impl
+ * or for tcgen05 with head dim 64. attn_backward is this with AUTO. */
+int attn_backward_ex(const void* Q, const void* K, const void* V,
+                     const void* O, const void* dO, const float* LSE,
+                     void* dQ, void* dK, void* dV,
+                     int B, int Hq, int Hkv, int Lq, int Lk, int d,
+                     int causal, float scale, const float* alibi_slopes,
+                     void* workspace, size_t workspace_bytes, int impl, void* stream);
+
 /*
  * attn_rmsnorm_matmul - RMSNorm followed by a matrix product, fused into one
  * kernel.

@@ -47,6 +47,9 @@ SIGNATURES = {
     "attn_backward_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
     "attn_backward": (_c_int, [_c_void_p] * 9 + [_c_int] * 7 + [_c_float, _c_void_p, _c_void_p,
                                                                ctypes.c_size_t, _c_void_p]),
+    "attn_backward_ex": (_c_int, [_c_void_p] * 9 + [_c_int] * 7 + [_c_float, _c_void_p, _c_void_p,
+                                                                  ctypes.c_size_t, _c_int,
+                                                                  _c_void_p]),
     "attn_rmsnorm_matmul": (_c_int, [_c_void_p] * 5 + [_c_int] * 3 + [_c_float, _c_int,
                                                                      _c_void_p]),
     "attn_rmsnorm_matmul_tiled": (_c_int, [_c_void_p] * 5 + [_c_int] * 3 + [_c_float, _c_int,
@@ -158,9 +161,10 @@ def prefill(q, k, v, causal=False, scale=None, alibi_slopes=None, impl="auto", o
 
 
 def backward(q, k, v, o, lse, dout, causal=False, scale=None, alibi_slopes=None,
-             workspace=None):
+             workspace=None, impl="auto"):
     """Gradients of prefill: returns (dQ, dK, dV) bf16; dK and dV are per KV
-    head (summed over a GQA group). `lse` is the forward's fp32 LSE."""
+    head (summed over a GQA group). `lse` is the forward's fp32 LSE. impl:
+    "auto" (tcgen05 for head dim 128), "tcgen05" or "mma_sync"."""
     for t, n in ((q, "q"), (o, "o"), (dout, "dout")):
         _req(t, n, torch.bfloat16, 4)
     _req(k, "k", torch.bfloat16, 4)
@@ -178,10 +182,11 @@ def backward(q, k, v, o, lse, dout, causal=False, scale=None, alibi_slopes=None,
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    st = lib().attn_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
-                             _ptr(dk), _ptr(dv), B, Hq, Hkv, Lq, Lk, d, int(bool(causal)),
-                             float(scale), _ptr(alibi_slopes), _ptr(workspace),
-                             workspace.numel() * workspace.element_size(), _stream())
+    st = lib().attn_backward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Lq, Lk, d,
+                                int(bool(causal)), float(scale), _ptr(alibi_slopes),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                IMPLS[impl], _stream())
     _check(st, "attn_backward")
     return dq, dk, dv
 

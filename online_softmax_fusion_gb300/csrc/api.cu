@@ -80,6 +80,22 @@ int make_map(CUtensorMap* m, const void* base, int d, int L, long long outer, in
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// fp32 tensor [outer, L, d] (d innermost, at most 256) as a 3-D tensor map
+// with a (d, box_rows, 1) box and no swizzle; the tcgen05 backward reduces
+// dQ tiles into it.
+int make_map_f32(CUtensorMap* m, const void* base, int d, int L, long long outer, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return ATTN_ERR_CUDA;
+    cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(L), cuuint64_t(outer)};
+    cuuint64_t strides[2] = {cuuint64_t(d) * 4, cuuint64_t(L) * cuuint64_t(d) * 4};
+    cuuint32_t box[3] = {cuuint32_t(d), cuuint32_t(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_common(int B, int Hq, int Hkv, int d, float scale) {
@@ -300,6 +316,16 @@ int attn_backward(const void* Q, const void* K, const void* V, const void* O, co
                   const float* LSE, void* dQ, void* dK, void* dV, int B, int Hq, int Hkv, int Lq,
                   int Lk, int d, int causal, float scale, const float* alibi_slopes,
                   void* workspace, size_t workspace_bytes, void* stream) {
+    return attn_backward_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, Lq, Lk, d, causal, scale,
+                            alibi_slopes, workspace, workspace_bytes, ATTN_IMPL_AUTO, stream);
+}
+
+int attn_backward_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                     const float* LSE, void* dQ, void* dK, void* dV, int B, int Hq, int Hkv,
+                     int Lq, int Lk, int d, int causal, float scale, const float* alibi_slopes,
+                     void* workspace, size_t workspace_bytes, int impl, void* stream) {
+    if (impl != ATTN_IMPL_AUTO && impl != ATTN_IMPL_TCGEN05 && impl != ATTN_IMPL_MMA_SYNC)
+        return ATTN_ERR_UNSUPPORTED;
     if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
         return ATTN_ERR_NULL;
     int st = check_common(B, Hq, Hkv, d, scale);
@@ -336,7 +362,22 @@ int attn_backward(const void* Q, const void* K, const void* V, const void* O, co
     p.scale_log2 = scale * kLog2e;
     p.causal = causal ? 1 : 0;
     if ((long long)(Lk + 63) / 64 > 0x7fffffffLL || Hkv > 65535) return ATTN_ERR_SHAPE;
-    return launch_backward(p, d, static_cast<cudaStream_t>(stream));
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const bool tc = impl == ATTN_IMPL_TCGEN05 || (impl == ATTN_IMPL_AUTO && d == 128);
+    if (!tc) return launch_backward(p, d, cs);
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    BwdTcLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    L.p = p;
+    L.p.status = status_ptr();
+    if ((st = make_map(&L.tmQ, Q, d, Lq, (long long)B * Hq, 64))) return st;
+    if ((st = make_map(&L.tmdO, dO, d, Lq, (long long)B * Hq, 64))) return st;
+    if ((st = make_map(&L.tmK, K, d, Lk, (long long)B * Hkv, 128))) return st;
+    if ((st = make_map(&L.tmV, V, d, Lk, (long long)B * Hkv, 128))) return st;
+    if ((st = make_map_f32(&L.tmdQ, p.dQacc, d, Lq, (long long)B * Hq, 64))) return st;
+    if ((st = launch_backward_prep(p, d, cs))) return st;
+    if ((st = launch_backward_tc_main(L, cs))) return st;
+    return launch_backward_convert(p, d, cs);
 }
 
 int attn_rmsnorm_matmul_splits(int B, int H, int D) {

@@ -303,19 +303,28 @@ int launch_main_d(const BwdParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-int launch_backward(const BwdParams& p, int d, cudaStream_t stream) {
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+int launch_backward_prep(const BwdParams& p, int d, cudaStream_t stream) {
     const long long rows = (long long)p.B * p.Hq * p.Lq;
     bwd_prep_kernel<<<unsigned((rows + 3) / 4), 128, 0, stream>>>(p.O, p.dO, p.Dsum, p.dQacc, rows,
                                                                   d);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    const int st = d == 64 ? launch_main_d<64>(p, stream) : launch_main_d<128>(p, stream);
-    if (st) return st;
-    const long long n2 = rows * d / 2;
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int launch_backward_convert(const BwdParams& p, int d, cudaStream_t stream) {
+    const long long n2 = (long long)p.B * p.Hq * p.Lq * d / 2;
     const long long want = (n2 + 255) / 256;
     const unsigned blocks = unsigned(want < 152LL * 32 ? want : 152LL * 32);
     bwd_convert_kernel<<<blocks, 256, 0, stream>>>(p.dQacc, p.dQ, n2, p.scale);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int launch_backward(const BwdParams& p, int d, cudaStream_t stream) {
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    int st = launch_backward_prep(p, d, stream);
+    if (st) return st;
+    st = d == 64 ? launch_main_d<64>(p, stream) : launch_main_d<128>(p, stream);
+    if (st) return st;
+    return launch_backward_convert(p, d, stream);
 }
 
 }  // namespace attn

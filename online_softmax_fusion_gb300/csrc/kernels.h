@@ -62,9 +62,23 @@ struct BwdParams {
     int B, Hq, Hkv, Lq, Lk, G;
     float scale, scale_log2;
     int causal;
+    int* status;                              // device status word (tcgen05 form)
 };
 
-int launch_backward(const BwdParams& p, int d, cudaStream_t stream);
+int launch_backward(const BwdParams& p, int d, cudaStream_t stream);   // mma.sync form
+// The pieces around the main kernel: D and a zeroed dQ accumulator; dQ from
+// the accumulator.
+int launch_backward_prep(const BwdParams& p, int d, cudaStream_t stream);
+int launch_backward_convert(const BwdParams& p, int d, cudaStream_t stream);
+
+// tcgen05 backward main kernel (head dim 128): Q / dO maps with 64-row boxes,
+// K / V maps with 128-row boxes (bf16, 128-byte swizzle), and the fp32 dQ
+// accumulator [B * Hq, Lq, 128] with a (128, 64) box, no swizzle.
+struct BwdTcLaunch {
+    CUtensorMap tmQ, tmK, tmV, tmdO, tmdQ;
+    BwdParams p;
+};
+int launch_backward_tc_main(const BwdTcLaunch& L, cudaStream_t stream);
 
 int launch_decode(const DecodeLaunch& L, int d, cudaStream_t stream);
 int launch_combine(const float* O_part, const float* LSE_part, int B, int Hq, int S, int d,

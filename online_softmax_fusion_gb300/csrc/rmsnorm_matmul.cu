@@ -257,8 +257,11 @@ __global__ void __launch_bounds__(kRmThreads, 2)
         const uint64_t b0d = tc::sdesc_sw128(smem_u32(xring), 16, 1024);
         for (int i = 0; i < nk; ++i) {
             const int sw = i % NW, sx = i % NX;
-            if (!mbar_wait(&sm.xready[sx], (i / NX) & 1, abort, p.status)) break;
-            if (!mbar_wait(&sm.wfull[sw], (i / NW) & 1, abort, p.status)) break;
+            // warp-uniform exits: the MMA issue below is warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.xready[sx], (i / NX) & 1, abort, p.status)))
+                break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.wfull[sw], (i / NW) & 1, abort, p.status)))
+                break;
             tc::fence_after_sync();
             const uint64_t wo = uint64_t((uint32_t(sw) * kWStageBytes) >> 4);
             const uint64_t xo = uint64_t((uint32_t(sx) * xbytes) >> 4);
@@ -405,7 +408,8 @@ __global__ void __launch_bounds__(kRmThreads, 2)
     __syncwarp();
     bool ok = true;
     if (warp >= kCvtWarp0) {
-        ok = mbar_wait(&sm.acc_full, 0, abort, p.status);
+        // warp-uniform, so the warp-collective TMEM loads below stay converged
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_full, 0, abort, p.status));
         tc::fence_after_sync();
     }
     __syncthreads();                          // this CTA's (E, s) rows are in sm.row_e / row_s
@@ -513,6 +517,7 @@ __global__ void __launch_bounds__(kRmThreads, 2)
     if (warp == 1) {
         volatile int never = 0;
         mbar_wait(&sm.acc_full, 0, &never, p.status);
+        __syncwarp();
         tc::fence_after_sync();
         tc::tmem_dealloc(tacc, ncols);
     }
