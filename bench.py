@@ -320,7 +320,7 @@ def measure_other_workloads(attn, W, dev, peaks):
     bwd = {"workload": PREFILL_WORKLOAD + " backward", "ms": t_bwd,
            "tflops": bfl / (t_bwd * 1e-3) / 1e12,
            "frac": bfl / (t_bwd * 1e-3) / 1e12 / peaks["bf16_tflops"],
-           "flops": bfl, "kernels": "prep + main (mma.sync) + convert"}
+           "flops": bfl, "kernels": "prep + main (tcgen05) + convert"}
     del pin, dout, O, LSE, ws
     dc = W.DECODE_CONFIGS["decode_long_outlier"]
     din = W.make_decode_inputs(dc, dev)
@@ -472,6 +472,37 @@ def run_rmsnorm(args):
                       "tflops": fl / (ms * 1e-3) / 1e12, "steps": args.steps,
                       "warmup": args.warmup, "timing": "eager launches, CUDA events"}),
           flush=True)
+    return 0
+
+
+# ------------------------------------------------------- backward only
+def run_backward(args):
+    """Times the attention backward alone on the causal MHA shape (H = 32,
+    L = 4096, d = 128) with --batch sequences: O and LSE from one forward,
+    then `warmup` untimed and `steps` timed backward calls."""
+    import torch
+    import online_softmax_fusion_gb300 as attn
+    import workloads as W
+    attn.lib()
+    peaks, _ = load_peaks()
+    base = W.PREFILL_CONFIGS[PREFILL_WORKLOAD]
+    cfg = W.PrefillConfig(f"{base.name}_b{args.batch}", B=args.batch, Hq=base.Hq, Hkv=base.Hkv,
+                          Lq=base.Lq, Lk=base.Lk, d=base.d, causal=True, seed=base.seed)
+    inp = W.make_prefill_inputs(cfg, "cuda")
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    dout = W._normal_bf16(q.shape, W.seeded_generator(cfg.seed + 7, "cuda"), "cuda")
+    O, LSE = attn.prefill(q, k, v, causal=True, scale=cfg.scale)
+    ws = torch.empty(attn.lib().attn_backward_workspace_bytes(cfg.B, cfg.Hq, cfg.Lq, cfg.d) // 4,
+                     dtype=torch.float32, device="cuda")
+    ms = time_launches(lambda: attn.backward(q, k, v, O, LSE, dout, causal=True, scale=cfg.scale,
+                                             workspace=ws),
+                       args.steps, args.warmup, torch.cuda.current_stream())
+    fl = backward_flops(cfg.B, cfg.Hq, cfg.Lq, cfg.Lk, cfg.d, True)
+    tf = fl / (ms * 1e-3) / 1e12
+    print(json.dumps({"metric": "attention backward TFLOP/s", "value": tf, "unit": "TFLOP/s",
+                      "workload": cfg.name, "ms_per_call": ms,
+                      "frac": tf / peaks["bf16_tflops"], "steps": args.steps,
+                      "warmup": args.warmup, "kernels": "prep + main + convert"}), flush=True)
     return 0
 
 
@@ -684,10 +715,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip the secondary GQA sweep / long-decode measurements")
-    ap.add_argument("--kernel", choices=["all", "prefill", "decode", "rmsnorm"], default="all",
+    ap.add_argument("--kernel", choices=["all", "prefill", "decode", "rmsnorm", "backward"],
+                    default="all",
                     help="time the whole step (default) or one kernel only (profiling)")
     ap.add_argument("--batch", type=int, default=16,
-                    help="batch rows of the RMSNorm + MatMul workload (--kernel rmsnorm)")
+                    help="batch rows of the RMSNorm + MatMul workload (--kernel rmsnorm), batch "
+                         "of the causal MHA backward (--kernel backward)")
     ap.add_argument("--small", action="store_true",
                     help="decode on a quarter of the batch (profiling captures)")
     args = ap.parse_args(argv)
@@ -697,6 +730,8 @@ def main(argv=None):
         return run_reference(args)
     if args.kernel == "rmsnorm":
         return run_rmsnorm(args)
+    if args.kernel == "backward":
+        return run_backward(args)
     return run_ours(args)
 
 

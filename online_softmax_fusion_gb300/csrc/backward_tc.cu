@@ -15,18 +15,20 @@
 //
 // CTA roles (384 threads):
 //   warp 0      TMA: K, V once; per step the Q and dO tiles (64 rows) into a
-//               2-slot ring, LSE and D of the 64 rows into the same slot
+//               4-slot ring, LSE and D of the 64 rows into the same slot
 //   warp 1      TMEM allocation; tcgen05.mma issue (one elected lane)
-//   warps 4-7   one thread per key (TMEM lane): P^T from S^T, P^T (bf16) back
-//               into TMEM for dV; dS^T from dP^T into shared memory (bf16)
-//               for dK and dQ^T; at the end dK
-//   warps 8-11  dQ^T from TMEM -> fp32 reductions into the accumulator (one
-//               thread per head dimension, 64 queries); at the end dV
+//   warps 4-11  two warpgroups, one thread per key (TMEM lane), each taking
+//               32 of the step's 64 query columns: P^T from S^T, P^T (bf16)
+//               back into TMEM for dV; dS^T from dP^T into shared memory
+//               (bf16) for dK and dQ^T; the previous step's dQ^T columns
+//               (TMEM lane = head dimension) added to the fp32 accumulator
+//               while dP^T is computed; at the end dK (warps 4-7) and dV
+//               (warps 8-11)
 // Tensor memory (512 columns): S^T double-buffered (2 x 64; P^T bf16 is
-// written over the upper half of its S^T), dP^T (64), dQ^T (64), dV (128),
+// written over S^T columns its group has read), dP^T (64), dQ^T (64), dV (128),
 // dK (128). S^T of the next step is computed while P^T of this step is
 // formed. Shared memory: K and V (resident, 128-byte swizzle), the ring and
-// dS^T double-buffered.
+// one dS^T tile.
 //
 // Issue order of the tensor core per step i:
 //   S_{i+1} | (P_i) dV_i | (dS_i) dP_{i+1}, dK_i, (dQ drained) dQ^T_i
@@ -42,7 +44,7 @@ namespace {
 constexpr int kBtThreads = 384;
 constexpr int kBtKeys = 128;                  // keys per CTA
 constexpr int kBtRows = 64;                   // query rows per step
-constexpr int kBtStages = 2;                  // Q / dO ring slots
+constexpr int kBtStages = 4;                  // Q / dO ring slots
 constexpr uint32_t kKVBox = 128 * 128;        // 128 keys x 64 dims (bf16, 128 B rows)
 constexpr uint32_t kQBox = 64 * 128;          // 64 rows x 64 dims
 // TMEM columns
@@ -56,7 +58,7 @@ struct BtSmem {
     alignas(1024) uint8_t k[2][kKVBox];                     // K block, dims 0-63 / 64-127
     alignas(1024) uint8_t v[2][kKVBox];
     alignas(1024) uint8_t qd[kBtStages][4][kQBox];          // per slot: Q (2 boxes), dO (2 boxes)
-    alignas(1024) uint8_t ds[2][kBtKeys * 128];             // dS^T [key][64 queries] bf16
+    alignas(1024) uint8_t ds[kBtKeys * 128];                // dS^T [key][64 queries] bf16
     float lse2[kBtStages][kBtRows];                         // LSE * log2(e); +inf = no weight
     float dsum[kBtStages][kBtRows];                         // D_i
     uint64_t kv_full;
@@ -65,8 +67,8 @@ struct BtSmem {
     uint64_t s_full[2];
     uint64_t dp_full;
     uint64_t p_full;
-    uint64_t ds_full[2];
-    uint64_t ds_free[2];
+    uint64_t ds_full;
+    uint64_t ds_free;
     uint64_t dq_full;
     uint64_t dq_free;
     uint64_t acc_done;
@@ -81,6 +83,17 @@ struct BtSmem {
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           int* status) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, status));
+}
+
+// Stores 32 lanes x 16 consecutive 32-bit columns (no wait).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        :
+        : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+          "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+          "r"(r[14]), "r"(r[15])
+        : "memory");
 }
 
 // 32 lanes x 64 consecutive 32-bit columns, then wait.
@@ -131,15 +144,13 @@ __global__ void __launch_bounds__(kBtThreads, 1)
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1);
         }
-        for (int c = 0; c < 2; ++c) {
-            mbar_init(&sm.s_full[c], 1);
-            mbar_init(&sm.ds_full[c], 4);
-            mbar_init(&sm.ds_free[c], 1);
-        }
+        for (int c = 0; c < 2; ++c) mbar_init(&sm.s_full[c], 1);
+        mbar_init(&sm.ds_full, 8);
+        mbar_init(&sm.ds_free, 1);
         mbar_init(&sm.dp_full, 1);
-        mbar_init(&sm.p_full, 4);
+        mbar_init(&sm.p_full, 8);
         mbar_init(&sm.dq_full, 1);
-        mbar_init(&sm.dq_free, 4);
+        mbar_init(&sm.dq_free, 8);
         mbar_init(&sm.acc_done, 1);
         sm.abort = 0;
         fence_mbar_init();
@@ -212,11 +223,10 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         const uint64_t dkT = tc::sdesc_sw128(smem_u32(sm.k[0]), kKVBox, 1024);      // K^T, MN-major
         const uint64_t dq0 = tc::sdesc_sw128(smem_u32(sm.qd[0][0]), 16, 1024);      // Q / dO K-major
         const uint64_t dqm = tc::sdesc_sw128(smem_u32(sm.qd[0][0]), kQBox, 1024);   // Q / dO MN-major
-        const uint64_t dsk = tc::sdesc_sw128(smem_u32(sm.ds[0]), 16, 1024);         // dS^T K-major
-        const uint64_t dsm = tc::sdesc_sw128(smem_u32(sm.ds[0]), 16384, 1024);      // dS^T MN-major
+        const uint64_t dsk = tc::sdesc_sw128(smem_u32(sm.ds), 16, 1024);            // dS^T K-major
+        const uint64_t dsm = tc::sdesc_sw128(smem_u32(sm.ds), 16384, 1024);         // dS^T MN-major
         constexpr uint32_t kSlot = (4 * kQBox) >> 4;     // ring slot stride (16-byte units)
         constexpr uint32_t kDO = (2 * kQBox) >> 4;       // dO after Q in a slot
-        constexpr uint32_t kDSb = (kBtKeys * 128) >> 4;  // dS^T buffer stride
         // A x B over K = 128 dims: 8 steps of 16, box switch after 4
         auto issue_qk = [&](uint64_t a0, uint64_t b0, uint32_t d) {
 #pragma unroll
@@ -256,15 +266,15 @@ __global__ void __launch_bounds__(kBtThreads, 1)
             if (!ok) break;
             tc::fence_after_sync();
             {
-                const uint32_t tP = tbase + kColS + (i & 1) * 64 + 32;
+                const uint32_t tP = tbase + kColS + (i & 1) * 64;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc::mma_bf16_ts_warp(tbase + kColDV, tP + kk * 8,
+                    tc::mma_bf16_ts_warp(tbase + kColDV, tP + (kk < 2 ? kk * 8 : 48 + (kk - 2) * 8),
                                          dqm + so + kDO + uint32_t(kk * (2048 >> 4)), idD,
                                          (i > 0 || kk > 0) ? 1u : 0u);
             }
             // dS^T of step i is in shared memory (and dP^T has been read)
-            ok = wait_warp(&sm.ds_full[i & 1], (i >> 1) & 1, abort, p.status);
+            ok = wait_warp(&sm.ds_full, i & 1, abort, p.status);
             if (!ok) break;
             tc::fence_after_sync();
             if (i + 1 < n) {
@@ -272,11 +282,10 @@ __global__ void __launch_bounds__(kBtThreads, 1)
                 issue_qk(dv_, dq0 + s1 + kDO, tbase + kColDP);
                 tc::commit_warp(&sm.dp_full);
             }
-            const uint32_t dso = uint32_t(i & 1) * kDSb;
             // dK += dS^T Q
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                tc::mma_bf16_ss_warp(tbase + kColDK, dsk + dso + uint32_t(kk * 2),
+                tc::mma_bf16_ss_warp(tbase + kColDK, dsk + uint32_t(kk * 2),
                                      dqm + so + uint32_t(kk * (2048 >> 4)), idD,
                                      (i > 0 || kk > 0) ? 1u : 0u);
             // dQ^T = K^T dS^T once the previous dQ^T has been drained
@@ -288,21 +297,48 @@ __global__ void __launch_bounds__(kBtThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 tc::mma_bf16_ss_warp(tbase + kColDQ, dkT + uint32_t(kk * (2048 >> 4)),
-                                     dsm + dso + uint32_t(kk * (2048 >> 4)), idQ, kk > 0);
+                                     dsm + uint32_t(kk * (2048 >> 4)), idQ, kk > 0);
             tc::commit_warp(&sm.dq_full);
             tc::commit_warp(&sm.empty[s]);
-            tc::commit_warp(&sm.ds_free[i & 1]);
+            tc::commit_warp(&sm.ds_free);
         }
         // covers every MMA issued above; the epilogue and TMEM release wait on it
         tc::commit_warp(&sm.acc_done);
-    } else if (warp >= 4 && warp < 8) {
-        // ========================================= P^T and dS^T (one key per thread)
+    } else if (warp >= 4) {
+        // ===================== P^T, dS^T and the dQ drain (one key per thread)
+        // Two warpgroups split the 64 query columns of a step: warps 4-7
+        // take columns 0-31, warps 8-11 columns 32-63 (same TMEM lanes).
+        const int half = warp >= 8 ? 1 : 0;
+        const int co = half * 32;                     // first query column of this group
         const int q4 = warp & 3;
-        const int kl = q4 * 32 + lane;                // key within the block
+        const int kl = q4 * 32 + lane;                // key within the block (TMEM lane)
         const int key = k0 + kl;
         const bool key_ok = key < p.Lk;
         const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+        // P^T (bf16) of this group's 32 queries goes over S^T columns this
+        // group has read and the other group never reads: columns 0-15
+        // (group 0) and 48-63 (group 1) of the step's S^T buffer
+        const uint32_t p_col = half ? 48u : 0u;
         bool ok = true;
+        // adds the dQ^T columns of this group for step j to the accumulator
+        // (TMEM lane = head dimension here)
+        auto drain_dq = [&](int j) -> bool {
+            if (!wait_warp(&sm.dq_full, j & 1, abort, p.status)) return false;
+            tc::fence_after_sync();
+            uint32_t v[32];
+            tc::tmem_ld_32x32b_x32(tbase + lane_off + kColDQ + co, v);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.dq_free);
+            int h, q0;
+            step_rows(j, h, q0);
+            float* dst = p.dQacc + ((size_t(b) * p.Hq + h) * p.Lq + q0 + co) * 128 + kl;
+            const int rows = min(32, p.Lq - q0 - co);
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                if (c < rows) atomicAdd(dst + size_t(c) * 128, __uint_as_float(v[c]));
+            return true;
+        };
         for (int i = 0; i < n; ++i) {
             const int s = i % kBtStages;
             int h, q0;
@@ -313,68 +349,86 @@ __global__ void __launch_bounds__(kBtThreads, 1)
             if (!ok) break;
             tc::fence_after_sync();
             const uint32_t tS = tbase + lane_off + kColS + (i & 1) * 64;
-            float x[64];
-            tmem_ld64(tS, x);
+            float x[32];
+            {
+                uint32_t r[32];
+                tc::tmem_ld_32x32b_x32(tS + co, r);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(r[c]);
+            }
             // rows of this step that some key of the block cannot see
             const bool diag = CAUSAL && (q0 + off < k0 + kBtKeys - 1);
-            const float* l2 = sm.lse2[s];
+            const float* l2 = sm.lse2[s] + co;
+            const int rq = q0 + co + off;             // aligned row of column 0
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
+            for (int c = 0; c < 32; ++c) {
                 float t = x[c] * p.scale_log2;
-                if (ALIBI) t -= slope_l2 * fabsf(float(q0 + c + off - key));
+                if (ALIBI) t -= slope_l2 * fabsf(float(rq + c - key));
                 float pr = ex2(t - l2[c]);
-                if (!key_ok || (diag && key > q0 + c + off)) pr = 0.f;
+                if (!key_ok || (diag && key > rq + c)) pr = 0.f;
                 x[c] = pr;
             }
             {
-                uint32_t pk[32];
+                uint32_t pk[16];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(x[2 * c], x[2 * c + 1]);
-                tc::tmem_st_32x32b_x32(tS + 32, pk);
+                for (int c = 0; c < 16; ++c) pk[c] = pack_bf16(x[2 * c], x[2 * c + 1]);
+                tmem_st16(tS + p_col, pk);
                 tc::tmem_wait_st();
             }
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.p_full);
+            // the previous step's dQ^T, while dP^T of this step is computed
+            if (i > 0 && !drain_dq(i - 1)) { ok = false; break; }
             // dS^T = P^T (dP^T - D)
             ok = wait_warp(&sm.dp_full, i & 1, abort, p.status);
             if (!ok) break;
             tc::fence_after_sync();
-            float dp[64];
-            tmem_ld64(tbase + lane_off + kColDP, dp);
-            const float* dd = sm.dsum[s];
+            {
+                uint32_t r[32];
+                tc::tmem_ld_32x32b_x32(tbase + lane_off + kColDP + co, r);
+                const float* dd = sm.dsum[s] + co;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) x[c] = x[c] * (dp[c] - dd[c]);
-            if (i >= 2) {
-                ok = wait_warp(&sm.ds_free[i & 1], ((i >> 1) - 1) & 1, abort, p.status);
+                for (int c = 0; c < 32; ++c) x[c] = x[c] * (__uint_as_float(r[c]) - dd[c]);
+            }
+            // the single dS^T buffer: dK and dQ^T of the previous step have
+            // completed (the dQ^T drain above already waited for them)
+            if (i >= 1) {
+                ok = wait_warp(&sm.ds_free, (i - 1) & 1, abort, p.status);
                 if (!ok) break;
             }
-            uint8_t* row = sm.ds[i & 1] + kl * 128;
+            uint8_t* row = sm.ds + kl * 128;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 uint4 w;
                 w.x = pack_bf16(x[8 * j + 0], x[8 * j + 1]);
                 w.y = pack_bf16(x[8 * j + 2], x[8 * j + 3]);
                 w.z = pack_bf16(x[8 * j + 4], x[8 * j + 5]);
                 w.w = pack_bf16(x[8 * j + 6], x[8 * j + 7]);
-                *reinterpret_cast<uint4*>(row + ((uint32_t(j) ^ (uint32_t(kl) & 7u)) << 4)) = w;
+                const uint32_t chunk = uint32_t(half * 4 + j);
+                *reinterpret_cast<uint4*>(row + ((chunk ^ (uint32_t(kl) & 7u)) << 4)) = w;
             }
             fence_proxy_async_smem();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.ds_full[i & 1]);
+            if (lane == 0) mbar_arrive(&sm.ds_full);
         }
-        // ---- dK (times the scale) of this block's keys; the TMEM loads are
-        //      warp-collective, so only the stores depend on the lane's key
+        if (ok && n > 0) ok = drain_dq(n - 1);
+        // ---- dK (times the scale, group 0) or dV (group 1) of this block's
+        //      keys; the TMEM loads are warp-collective, so only the stores
+        //      depend on the lane's key
         if (ok) ok = wait_warp(&sm.acc_done, 0, abort, p.status);
         tc::fence_after_sync();
         if (__all_sync(0xffffffffu, ok && !*abort)) {
-            __nv_bfloat16* dst = p.dK + ((size_t(b) * p.Hkv + kvh) * p.Lk + (key_ok ? key : 0)) * 128;
+            const float mul = half ? 1.f : p.scale;
+            __nv_bfloat16* dst = (half ? p.dV : p.dK) +
+                                 ((size_t(b) * p.Hkv + kvh) * p.Lk + (key_ok ? key : 0)) * 128;
+            const uint32_t col = half ? kColDV : kColDK;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t r[32];
                 if (n > 0) {
-                    tc::tmem_ld_32x32b_x32(tbase + lane_off + kColDK + c * 32, r);
+                    tc::tmem_ld_32x32b_x32(tbase + lane_off + col + c * 32, r);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r[e] = 0u;
@@ -382,65 +436,14 @@ __global__ void __launch_bounds__(kBtThreads, 1)
 #pragma unroll
                 for (int v8 = 0; v8 < 4; ++v8) {
                     uint4 w;
-                    w.x = pack_bf16(__uint_as_float(r[v8 * 8 + 0]) * p.scale,
-                                    __uint_as_float(r[v8 * 8 + 1]) * p.scale);
-                    w.y = pack_bf16(__uint_as_float(r[v8 * 8 + 2]) * p.scale,
-                                    __uint_as_float(r[v8 * 8 + 3]) * p.scale);
-                    w.z = pack_bf16(__uint_as_float(r[v8 * 8 + 4]) * p.scale,
-                                    __uint_as_float(r[v8 * 8 + 5]) * p.scale);
-                    w.w = pack_bf16(__uint_as_float(r[v8 * 8 + 6]) * p.scale,
-                                    __uint_as_float(r[v8 * 8 + 7]) * p.scale);
-                    if (key_ok) *reinterpret_cast<uint4*>(dst + c * 32 + v8 * 8) = w;
-                }
-            }
-        }
-        tc::fence_before_sync();
-    } else if (warp >= 8) {
-        // ============================================ dQ^T drain and dV
-        const int q4 = warp & 3;
-        const int dim = q4 * 32 + lane;               // head dimension (TMEM lane)
-        const uint32_t lane_off = uint32_t(q4 * 32) << 16;
-        bool ok = true;
-        for (int i = 0; i < n; ++i) {
-            ok = wait_warp(&sm.dq_full, i & 1, abort, p.status);
-            if (!ok) break;
-            tc::fence_after_sync();
-            float v[64];
-            tmem_ld64(tbase + lane_off + kColDQ, v);
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.dq_free);
-            int h, q0;
-            step_rows(i, h, q0);
-            float* dst = p.dQacc + ((size_t(b) * p.Hq + h) * p.Lq + q0) * 128 + dim;
-            const int rows = min(kBtRows, p.Lq - q0);
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-                if (c < rows) atomicAdd(dst + size_t(c) * 128, v[c]);
-        }
-        // ---- dV of this block's keys (TMEM lane = key here)
-        if (ok) ok = wait_warp(&sm.acc_done, 0, abort, p.status);
-        tc::fence_after_sync();
-        const int key = k0 + dim;
-        const bool key_ok = key < p.Lk;
-        if (__all_sync(0xffffffffu, ok && !*abort)) {
-            __nv_bfloat16* dst = p.dV + ((size_t(b) * p.Hkv + kvh) * p.Lk + (key_ok ? key : 0)) * 128;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                if (n > 0) {
-                    tc::tmem_ld_32x32b_x32(tbase + lane_off + kColDV + c * 32, r);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = 0u;
-                }
-#pragma unroll
-                for (int v8 = 0; v8 < 4; ++v8) {
-                    uint4 w;
-                    w.x = pack_bf16(__uint_as_float(r[v8 * 8 + 0]), __uint_as_float(r[v8 * 8 + 1]));
-                    w.y = pack_bf16(__uint_as_float(r[v8 * 8 + 2]), __uint_as_float(r[v8 * 8 + 3]));
-                    w.z = pack_bf16(__uint_as_float(r[v8 * 8 + 4]), __uint_as_float(r[v8 * 8 + 5]));
-                    w.w = pack_bf16(__uint_as_float(r[v8 * 8 + 6]), __uint_as_float(r[v8 * 8 + 7]));
+                    w.x = pack_bf16(__uint_as_float(r[v8 * 8 + 0]) * mul,
+                                    __uint_as_float(r[v8 * 8 + 1]) * mul);
+                    w.y = pack_bf16(__uint_as_float(r[v8 * 8 + 2]) * mul,
+                                    __uint_as_float(r[v8 * 8 + 3]) * mul);
+                    w.z = pack_bf16(__uint_as_float(r[v8 * 8 + 4]) * mul,
+                                    __uint_as_float(r[v8 * 8 + 5]) * mul);
+                    w.w = pack_bf16(__uint_as_float(r[v8 * 8 + 6]) * mul,
+                                    __uint_as_float(r[v8 * 8 + 7]) * mul);
                     if (key_ok) *reinterpret_cast<uint4*>(dst + c * 32 + v8 * 8) = w;
                 }
             }
