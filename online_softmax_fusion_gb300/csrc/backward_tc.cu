@@ -76,15 +76,6 @@ struct BtSmem {
     int abort;
 };
 
-// A bounded wait whose result is the same in every lane of the warp, so that
-// the warp stays converged for the warp-collective tcgen05 instructions that
-// follow (a lane that saw the phase complete and one that saw the abort flag
-// take the same path).
-__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* status) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, status));
-}
-
 // Stores 32 lanes x 16 consecutive 32-bit columns (no wait).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
@@ -236,10 +227,10 @@ __global__ void __launch_bounds__(kBtThreads, 1)
                 tc::mma_bf16_ss_warp(d, a0 + oa, b0 + ob, idS, kk > 0);
             }
         };
-        bool ok = wait_warp(&sm.kv_full, 0, abort, p.status);
+        bool ok = mbar_wait_warp(&sm.kv_full, 0, abort, p.status);
         tc::fence_after_sync();
         auto wait_full = [&](int i) {
-            ok = ok && wait_warp(&sm.full[i % kBtStages], (i / kBtStages) & 1, abort, p.status);
+            ok = ok && mbar_wait_warp(&sm.full[i % kBtStages], (i / kBtStages) & 1, abort, p.status);
             tc::fence_after_sync();
         };
         if (ok && n > 0) {
@@ -262,7 +253,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
                 tc::commit_warp(&sm.s_full[(i + 1) & 1]);
             }
             // dV += P^T dO (P^T bf16 in TMEM over the upper half of S^T)
-            ok = wait_warp(&sm.p_full, i & 1, abort, p.status);
+            ok = mbar_wait_warp(&sm.p_full, i & 1, abort, p.status);
             if (!ok) break;
             tc::fence_after_sync();
             {
@@ -274,7 +265,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
                                          (i > 0 || kk > 0) ? 1u : 0u);
             }
             // dS^T of step i is in shared memory (and dP^T has been read)
-            ok = wait_warp(&sm.ds_full, i & 1, abort, p.status);
+            ok = mbar_wait_warp(&sm.ds_full, i & 1, abort, p.status);
             if (!ok) break;
             tc::fence_after_sync();
             if (i + 1 < n) {
@@ -290,7 +281,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
                                      (i > 0 || kk > 0) ? 1u : 0u);
             // dQ^T = K^T dS^T once the previous dQ^T has been drained
             if (i > 0) {
-                ok = wait_warp(&sm.dq_free, (i - 1) & 1, abort, p.status);
+                ok = mbar_wait_warp(&sm.dq_free, (i - 1) & 1, abort, p.status);
                 if (!ok) break;
                 tc::fence_after_sync();
             }
@@ -323,7 +314,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         // adds the dQ^T columns of this group for step j to the accumulator
         // (TMEM lane = head dimension here)
         auto drain_dq = [&](int j) -> bool {
-            if (!wait_warp(&sm.dq_full, j & 1, abort, p.status)) return false;
+            if (!mbar_wait_warp(&sm.dq_full, j & 1, abort, p.status)) return false;
             tc::fence_after_sync();
             uint32_t v[32];
             tc::tmem_ld_32x32b_x32(tbase + lane_off + kColDQ + co, v);
@@ -344,8 +335,8 @@ __global__ void __launch_bounds__(kBtThreads, 1)
             int h, q0;
             step_rows(i, h, q0);
             const float slope_l2 = ALIBI ? p.slopes[h] * kLog2e : 0.f;
-            ok = wait_warp(&sm.s_full[i & 1], (i >> 1) & 1, abort, p.status);
-            ok = ok && wait_warp(&sm.full[s], (i / kBtStages) & 1, abort, p.status);
+            ok = mbar_wait_warp(&sm.s_full[i & 1], (i >> 1) & 1, abort, p.status);
+            ok = ok && mbar_wait_warp(&sm.full[s], (i / kBtStages) & 1, abort, p.status);
             if (!ok) break;
             tc::fence_after_sync();
             const uint32_t tS = tbase + lane_off + kColS + (i & 1) * 64;
@@ -381,7 +372,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
             // the previous step's dQ^T, while dP^T of this step is computed
             if (i > 0 && !drain_dq(i - 1)) { ok = false; break; }
             // dS^T = P^T (dP^T - D)
-            ok = wait_warp(&sm.dp_full, i & 1, abort, p.status);
+            ok = mbar_wait_warp(&sm.dp_full, i & 1, abort, p.status);
             if (!ok) break;
             tc::fence_after_sync();
             {
@@ -394,7 +385,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
             // the single dS^T buffer: dK and dQ^T of the previous step have
             // completed (the dQ^T drain above already waited for them)
             if (i >= 1) {
-                ok = wait_warp(&sm.ds_free, (i - 1) & 1, abort, p.status);
+                ok = mbar_wait_warp(&sm.ds_free, (i - 1) & 1, abort, p.status);
                 if (!ok) break;
             }
             uint8_t* row = sm.ds + kl * 128;
@@ -417,7 +408,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         // ---- dK (times the scale, group 0) or dV (group 1) of this block's
         //      keys; the TMEM loads are warp-collective, so only the stores
         //      depend on the lane's key
-        if (ok) ok = wait_warp(&sm.acc_done, 0, abort, p.status);
+        if (ok) ok = mbar_wait_warp(&sm.acc_done, 0, abort, p.status);
         tc::fence_after_sync();
         if (__all_sync(0xffffffffu, ok && !*abort)) {
             const float mul = half ? 1.f : p.scale;

@@ -93,6 +93,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     return mbar_wait_limit(bar, parity, abort, status, kWaitLimitNs);
 }
 
+// The same wait executed by a whole warp with one result for every lane: a
+// lane that saw the phase complete and one that saw the abort flag take the
+// same path, so the warp stays converged for the warp-collective instructions
+// that follow (ldmatrix, mma.sync, tcgen05.ld/st/mma).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort, int* status) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, status));
+}
+
 // ----------------------------------------------------------------------- TMA
 // 3-D tiled bulk-tensor load global -> shared, completion counted in bytes on
 // `bar`. The innermost coordinate x must be a multiple of 8 elements (16 B).

@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kDecThreads)
         const int t4 = lane & 3;
         for (int it = 0; it < ntiles; ++it) {
             const int st = it % kDecStages;
-            if (!mbar_wait(&sm.full[st], (it / kDecStages) & 1, abort, p.status)) break;
+            if (!mbar_wait_warp(&sm.full[st], (it / kDecStages) & 1, abort, p.status)) break;
             const uint8_t* kt = &sm.kv[st][0][0][0];
             const uint8_t* vt = &sm.kv[st][1][0][0];
 

@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kMmaThreads)
                 issued = it + 1;
             }
         }
-    } else if (mbar_wait(&sm.qfull, 0, abort, p.status)) {
+    } else if (mbar_wait_warp(&sm.qfull, 0, abort, p.status)) {
         const int g = lane >> 2, t4 = lane & 3;
         uint32_t qa[D / 16][4];
 #pragma unroll
@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kMmaThreads)
 
         for (int it = 0; it < ntiles; ++it) {
             const int st = it % kMmaStages;
-            if (!mbar_wait(&sm.full[st], (it / kMmaStages) & 1, abort, p.status)) break;
+            if (!mbar_wait_warp(&sm.full[st], (it / kMmaStages) & 1, abort, p.status)) break;
             const uint8_t* kt = &sm.kv[st][0][0][0];
             const uint8_t* vt = &sm.kv[st][1][0][0];
 

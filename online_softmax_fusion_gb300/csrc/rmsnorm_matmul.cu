@@ -257,11 +257,8 @@ __global__ void __launch_bounds__(kRmThreads, 2)
         const uint64_t b0d = tc::sdesc_sw128(smem_u32(xring), 16, 1024);
         for (int i = 0; i < nk; ++i) {
             const int sw = i % NW, sx = i % NX;
-            // warp-uniform exits: the MMA issue below is warp-collective
-            if (!__all_sync(0xffffffffu, mbar_wait(&sm.xready[sx], (i / NX) & 1, abort, p.status)))
-                break;
-            if (!__all_sync(0xffffffffu, mbar_wait(&sm.wfull[sw], (i / NW) & 1, abort, p.status)))
-                break;
+            if (!mbar_wait_warp(&sm.xready[sx], (i / NX) & 1, abort, p.status)) break;
+            if (!mbar_wait_warp(&sm.wfull[sw], (i / NW) & 1, abort, p.status)) break;
             tc::fence_after_sync();
             const uint64_t wo = uint64_t((uint32_t(sw) * kWStageBytes) >> 4);
             const uint64_t xo = uint64_t((uint32_t(sx) * xbytes) >> 4);
@@ -296,7 +293,7 @@ __global__ void __launch_bounds__(kRmThreads, 2)
             float SC2 = 0.f;        // 2^-2E, set whenever E changes
             for (int i = grp; i < nk; i += ngroups) {
                 const int s = i % NX;
-                if (!mbar_wait(&sm.xfull[s], (i / NX) & 1, abort, p.status)) break;
+                if (!mbar_wait_warp(&sm.xfull[s], (i / NX) & 1, abort, p.status)) break;
                 if (r < NB) {
                     uint8_t* row = xring + size_t(s) * xbytes + r * 128;
                     const uint32_t sw = uint32_t(r) & 7u;
@@ -408,8 +405,7 @@ __global__ void __launch_bounds__(kRmThreads, 2)
     __syncwarp();
     bool ok = true;
     if (warp >= kCvtWarp0) {
-        // warp-uniform, so the warp-collective TMEM loads below stay converged
-        ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_full, 0, abort, p.status));
+        ok = mbar_wait_warp(&sm.acc_full, 0, abort, p.status);
         tc::fence_after_sync();
     }
     __syncthreads();                          // this CTA's (E, s) rows are in sm.row_e / row_s
