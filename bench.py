@@ -63,6 +63,21 @@ def prefill_flops(B, Hq, Lq, Lk, d, causal) -> int:
     return 4 * d * B * Hq * pairs
 
 
+def window_pairs(Lq: int, Lk: int, left: int, right: int, causal: bool) -> int:
+    """Unmasked (query, key) pairs of one head under a sliding window: aligned
+    row i' = i + Lk - Lq sees keys [i' - left, i' + right] (a negative bound
+    is unlimited on that side), and with causal keys after i' stay masked."""
+    import numpy as np
+    i = np.arange(Lq, dtype=np.int64) + (Lk - Lq)
+    lo = np.zeros_like(i) if left < 0 else np.maximum(0, i - left)
+    hi = np.full_like(i, Lk - 1)
+    if right >= 0:
+        hi = np.minimum(hi, i + right)
+    if causal:
+        hi = np.minimum(hi, i)
+    return int(np.maximum(0, hi - lo + 1).sum())
+
+
 def backward_flops(B, Hq, Lq, Lk, d, causal) -> int:
     """Five products per unmasked pair (S recomputed, dP, dV, dK, dQ): 10*d."""
     pairs = causal_pairs(Lq, Lk) if causal else Lq * Lk
@@ -305,6 +320,23 @@ def measure_other_workloads(attn, W, dev, peaks):
         sweep.append({"L": L, "ms": ms, "tflops": tf, "frac": tf / peaks["bf16_tflops"],
                       "inputs_exceed_l2": in_bytes > 129e6, "timing": "cuda graph replay"})
         del inp, O, LSE
+    # SoftCap and a causal sliding window on the causal MHA workload
+    pc = W.PREFILL_CONFIGS[PREFILL_WORKLOAD]
+    pin = W.make_prefill_inputs(pc, dev)
+    Ov = torch.empty_like(pin["q"])
+    Lv = torch.empty((pc.B, pc.Hq, pc.Lq), dtype=torch.float32, device=dev)
+    variants = []
+    for name, cap, win in (("softcap_30", 30.0, (-1, -1)), ("window_left_1024", 0.0, (1024, -1))):
+        ms = graph_time(lambda: attn.prefill(pin["q"], pin["k"], pin["v"], causal=True,
+                                             scale=pc.scale, out=Ov, lse=Lv, softcap=cap,
+                                             window=win), 4, replays=3)
+        pairs = window_pairs(pc.Lq, pc.Lk, win[0], win[1], True)
+        fl = 4 * pc.d * pc.B * pc.Hq * pairs
+        tf = fl / (ms * 1e-3) / 1e12
+        variants.append({"variant": name, "ms": ms, "tflops": tf,
+                         "frac": tf / peaks["bf16_tflops"], "flops": fl,
+                         "workload": PREFILL_WORKLOAD, "timing": "cuda graph replay"})
+    del pin, Ov, Lv
     # backward of the causal MHA workload (forward outputs as its inputs)
     pc = W.PREFILL_CONFIGS[PREFILL_WORKLOAD]
     pin = W.make_prefill_inputs(pc, dev)
@@ -363,7 +395,8 @@ def measure_other_workloads(attn, W, dev, peaks):
                     "timing": "cuda graph replay, W rotated over 5 copies (> L2)"})
         del rin, wcopies, Orm
     return {"prefill_gqa_alibi_sweep": sweep, "decode_long_outlier": long_dec,
-            "backward_causal_mha_4k": bwd, "rmsnorm_matmul": rms}
+            "backward_causal_mha_4k": bwd, "rmsnorm_matmul": rms,
+            "prefill_softcap_window": variants}
 
 
 # ------------------------------------------------------------ CPU oracle

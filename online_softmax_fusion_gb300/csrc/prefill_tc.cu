@@ -328,11 +328,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(rr[i]);
             }
             const int k0 = j * 128;
-            const bool need_mask = EXTRA || (k0 + 128 > p.Lk) ||
-                                   (CAUSAL && k0 + 127 > row0 + q4 * 32 + off);
+            // aligned index of this warp's first row: the warp's 32 rows need
+            // per-key masks only on tiles that cross the key length, the
+            // causal diagonal or a window edge (warp-uniform)
+            const int w_al = row0 + q4 * 32 + off;
+            bool need_mask = (k0 + 128 > p.Lk) || (CAUSAL && k0 + 127 > w_al);
+            if (EXTRA) {
+                if (p.window_left >= 0 && k0 < w_al + 31 - p.window_left) need_mask = true;
+                if (p.window_right >= 0 && k0 + 127 > w_al + p.window_right) need_mask = true;
+            }
+            const bool cap = EXTRA && p.softcap > 0.f;
             // x = s * scale (log2 domain) + bias, masked; on unmasked tiles
             // without bias the scale is folded into the exp's FMA below
-            const bool fast = !need_mask && !ALIBI && sl2 > 0.f;
+            const bool fast = !need_mask && !ALIBI && !cap && sl2 > 0.f;
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (fast) {
 #pragma unroll
@@ -342,7 +350,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mx4[2] = max3(mx4[2], s[c + 4], s[c + 5]);
                     mx4[3] = max3(mx4[3], s[c + 6], s[c + 7]);
                 }
-            } else if (ALIBI && CAUSAL && !need_mask) {
+            } else if (ALIBI && CAUSAL && !need_mask && !cap) {
                 // every key of this tile is at or before every row of the
                 // warp: bias = slope * (key - i'), built from an exact integer
                 // counter c and one packed FMA per key pair, then fused into
@@ -360,33 +368,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mx4[(c >> 1) & 3] = max3(mx4[(c >> 1) & 3], s[c], s[c + 1]);
                     cc2 = f2_add(cc2, two2);
                 }
-            } else {
+            } else if (cap && !need_mask && !ALIBI) {
+                // unmasked tile with the cap: x = cap * tanh(score / cap), the
+                // same formula as the general path below without its masks
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const int key = k0 + c;
-                    float x;
-                    if (EXTRA && p.softcap > 0.f) {
+                for (int c = 0; c < 128; c += 2) {
+                    const float y0 = fminf(fmaxf(s[c] * sc_div, -15.f), 15.f);
+                    const float y1 = fminf(fmaxf(s[c + 1] * sc_div, -15.f), 15.f);
+                    const float e0 = ex2(y0 * (2.f * kLog2e));
+                    const float e1 = ex2(y1 * (2.f * kLog2e));
+                    s[c] = cap_l2 * ((e0 - 1.f) * rcp_approx(e0 + 1.f));
+                    s[c + 1] = cap_l2 * ((e1 - 1.f) * rcp_approx(e1 + 1.f));
+                    mx4[(c >> 1) & 3] = max3(mx4[(c >> 1) & 3], s[c], s[c + 1]);
+                }
+            } else {
+                // general tile: this row's visible keys form one interval
+                // [klo, khi] (key length, causal, window), computed once per
+                // tile; per key only the transform, the bias and one range test
+                int khi = p.Lk - 1;
+                if (CAUSAL) khi = min(khi, i_al);
+                int klo = 0;
+                if (EXTRA) {
+                    if (p.window_left >= 0) klo = max(klo, i_al - p.window_left);
+                    if (p.window_right >= 0) khi = min(khi, i_al + p.window_right);
+                }
+                const int clo = klo - k0, chi = khi - k0;
+                if (cap) {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) {
                         // cap * tanh(score / cap), tanh(y) = (e - 1) / (e + 1)
                         // with e = 2^(2 y log2 e); |y| <= 15 keeps e finite
                         // and tanh(15) rounds to 1 in fp32
                         const float y = fminf(fmaxf(s[c] * sc_div, -15.f), 15.f);
                         const float e = ex2(y * (2.f * kLog2e));
-                        x = cap_l2 * ((e - 1.f) * rcp_approx(e + 1.f));
-                    } else {
-                        x = s[c] * sl2;
+                        float x = cap_l2 * ((e - 1.f) * rcp_approx(e + 1.f));
+                        if (ALIBI) {
+                            const float dist = float(i_al - (k0 + c));
+                            x -= slope_l2 * (CAUSAL ? dist : fabsf(dist));
+                        }
+                        if (c < clo || c > chi) x = -INFINITY;
+                        s[c] = x;
+                        mx4[c & 3] = fmaxf(mx4[c & 3], x);
                     }
-                    if (ALIBI) {
-                        const float dist = float(i_al - key);
-                        x -= slope_l2 * (CAUSAL ? dist : fabsf(dist));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) {
+                        float x = s[c] * sl2;
+                        if (ALIBI) {
+                            const float dist = float(i_al - (k0 + c));
+                            x -= slope_l2 * (CAUSAL ? dist : fabsf(dist));
+                        }
+                        if (c < clo || c > chi) x = -INFINITY;
+                        s[c] = x;
+                        mx4[c & 3] = fmaxf(mx4[c & 3], x);
                     }
-                    bool masked = key >= p.Lk || (CAUSAL && key > i_al);
-                    if (EXTRA) {
-                        masked = masked || (p.window_left >= 0 && key < i_al - p.window_left) ||
-                                 (p.window_right >= 0 && key > i_al + p.window_right);
-                    }
-                    if (masked) x = -INFINITY;
-                    s[c] = x;
-                    mx4[c & 3] = fmaxf(mx4[c & 3], x);
                 }
             }
             float mx = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));

@@ -127,3 +127,20 @@ def test_rmsnorm_matmul_traffic_is_the_weight_at_small_batch():
     b = bench.rmsnorm_matmul_bytes(1, 4096, 4096)
     assert 32 * 2 ** 20 <= b <= 32 * 2 ** 20 + 64 * 1024
     assert bench.rmsnorm_matmul_flops(256, 4096, 4096) == 2 * 256 * 4096 * 4096
+
+
+@pytest.mark.parametrize("Lq,Lk,left,right,causal", [
+    (7, 7, 2, -1, True), (7, 9, 3, 1, False), (9, 5, -1, 2, False), (6, 6, -1, -1, True),
+    (5, 8, 0, 0, False), (8, 8, 10, -1, True)])
+def test_window_pairs_brute_force(Lq, Lk, left, right, causal):
+    n = 0
+    for i in range(Lq):
+        ia = i + Lk - Lq
+        for j in range(Lk):
+            ok = (left < 0 or j >= ia - left) and (right < 0 or j <= ia + right)
+            if causal:
+                ok = ok and j <= ia
+            n += ok
+    assert bench.window_pairs(Lq, Lk, left, right, causal) == n
+    if left < 0 and right < 0 and causal:
+        assert n == bench.causal_pairs(Lq, Lk)
