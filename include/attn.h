@@ -166,6 +166,24 @@ int attn_backward_ex(const void* Q, const void* K, const void* V,
                      void* workspace, size_t workspace_bytes, int impl, void* stream);
 
 /*
+ * attn_prefill_splitkv - the tcgen05 prefill with each CTA's KV range split
+ * into num_splits chunks (grid z), each writing the split-K partials of
+ * Neptune论文浅读 §6 (O_s = o / l in fp32 and LSE_s = m + ln l), merged by the
+ * log-sum-exp combine of attn_combine with query rows in the role of heads.
+ * For low-occupancy shapes (few rows x heads). Causal / ALiBi / GQA as in
+ * attn_prefill; no softcap or window. num_splits 1 is attn_prefill itself;
+ * 2..16 need a workspace of attn_prefill_splitkv_workspace_bytes() (fp32
+ * [B, Hq, Lq, S, d] then [B, Hq, Lq, S], 16-byte aligned). ATTN_ERR_WORKSPACE
+ * for num_splits outside 1..16 or a short workspace; other errors as
+ * attn_prefill.
+ */
+size_t attn_prefill_splitkv_workspace_bytes(int B, int Hq, int Lq, int d, int num_splits);
+int attn_prefill_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                         int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal, float scale,
+                         const float* alibi_slopes, int num_splits, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
  * attn_rmsnorm_matmul - RMSNorm followed by a matrix product, fused into one
  * kernel.
  *

@@ -44,6 +44,10 @@ SIGNATURES = {
                                                                    _c_void_p]),
     "attn_prefill_opts": (_c_int, [_c_void_p] * 5 + [_c_int] * 6 + [ctypes.POINTER(PrefillOptions),
                                                                      _c_void_p]),
+    "attn_prefill_splitkv_workspace_bytes": (ctypes.c_size_t, [_c_int] * 5),
+    "attn_prefill_splitkv": (_c_int, [_c_void_p] * 5 + [_c_int] * 7 + [_c_float, _c_void_p, _c_int,
+                                                                     _c_void_p, ctypes.c_size_t,
+                                                                     _c_void_p]),
     "attn_backward_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
     "attn_backward": (_c_int, [_c_void_p] * 9 + [_c_int] * 7 + [_c_float, _c_void_p, _c_void_p,
                                                                ctypes.c_size_t, _c_void_p]),
@@ -157,6 +161,35 @@ def prefill(q, k, v, causal=False, scale=None, alibi_slopes=None, impl="auto", o
                                    Lq, Lk, d, int(bool(causal)), float(scale), _ptr(alibi_slopes),
                                    IMPLS[impl], _stream())
     _check(st, "attn_prefill")
+    return out, lse
+
+
+def prefill_splitkv(q, k, v, num_splits, causal=False, scale=None, alibi_slopes=None, out=None,
+                    lse=None, with_lse=True, workspace=None):
+    """prefill with each CTA's KV range split num_splits ways and merged by
+    the log-sum-exp combine. Returns (O, LSE or None)."""
+    _req(q, "q", torch.bfloat16, 4)
+    _req(k, "k", torch.bfloat16, 4)
+    _req(v, "v", torch.bfloat16, 4)
+    B, Hq, Lq, d = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if alibi_slopes is not None:
+        _req(alibi_slopes, "alibi_slopes", torch.float32, 1)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and with_lse:
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    nbytes = lib().attn_prefill_splitkv_workspace_bytes(B, Hq, Lq, d, int(num_splits))
+    if workspace is None and nbytes:
+        workspace = torch.empty(nbytes // 4, dtype=torch.float32, device=q.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().attn_prefill_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv,
+                                    Lq, Lk, d, int(bool(causal)), float(scale),
+                                    _ptr(alibi_slopes), int(num_splits), _ptr(workspace), wsb,
+                                    _stream())
+    _check(st, "attn_prefill_splitkv")
     return out, lse
 
 

@@ -283,6 +283,62 @@ int prefill_impl(const void* Q, const void* K, const void* V, void* O, float* LS
 
 extern "C" {
 
+size_t attn_prefill_splitkv_workspace_bytes(int B, int Hq, int Lq, int d, int num_splits) {
+    if (B <= 0 || Hq <= 0 || Lq <= 0 || d <= 0 || num_splits <= 1) return 0;
+    return size_t(B) * Hq * Lq * size_t(num_splits) * size_t(d + 1) * sizeof(float);
+}
+
+int attn_prefill_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                         int Hq, int Hkv, int Lq, int Lk, int d, int causal, float scale,
+                         const float* alibi_slopes, int num_splits, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    if (num_splits < 1 || num_splits > 16) return ATTN_ERR_WORKSPACE;
+    if (num_splits == 1)
+        return prefill_impl(Q, K, V, O, LSE, B, Hq, Hkv, Lq, Lk, d, causal, scale, alibi_slopes,
+                            0.f, -1, -1, ATTN_IMPL_TCGEN05, stream);
+    if (!Q || !K || !V || !O || !workspace) return ATTN_ERR_NULL;
+    int st = check_common(B, Hq, Hkv, d, scale);
+    if (st) return st;
+    if (Lq <= 0 || Lk <= 0) return ATTN_ERR_SHAPE;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(workspace))
+        return ATTN_ERR_ALIGN;
+    if ((LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) ||
+        (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)))
+        return ATTN_ERR_ALIGN;
+    if (workspace_bytes < attn_prefill_splitkv_workspace_bytes(B, Hq, Lq, d, num_splits))
+        return ATTN_ERR_WORKSPACE;
+    PrefillLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    L.p.O = static_cast<__nv_bfloat16*>(O);
+    L.p.LSE = LSE;
+    L.p.slopes = alibi_slopes;
+    L.p.B = B;
+    L.p.Hq = Hq;
+    L.p.Hkv = Hkv;
+    L.p.Lq = Lq;
+    L.p.Lk = Lk;
+    L.p.G = Hq / Hkv;
+    L.p.scale_log2 = scale * kLog2e;
+    L.p.causal = causal ? 1 : 0;
+    L.p.softcap = 0.f;
+    L.p.window_left = -1;
+    L.p.window_right = -1;
+    L.p.pair_heads = (L.p.G % 2 == 0) ? 1 : 0;
+    L.p.splits = num_splits;
+    L.p.O_part = static_cast<float*>(workspace);
+    L.p.LSE_part = L.p.O_part + size_t(B) * Hq * Lq * size_t(num_splits) * d;
+    L.p.status = status_ptr();
+    if (!L.p.status) return ATTN_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = make_map(&L.tmQ, Q, d, Lq, (long long)B * Hq, kTcBM))) return st;
+    if ((st = make_map(&L.tmK, K, d, Lk, (long long)B * Hkv, kTcBN))) return st;
+    if ((st = make_map(&L.tmV, V, d, Lk, (long long)B * Hkv, kTcBN))) return st;
+    if ((st = launch_prefill_tc(L, d, s))) return st;
+    // the partials of each row merged with the split-K combine (rows act as heads)
+    if ((long long)B * Hq > 0x7fffffffLL / Lq) return ATTN_ERR_SHAPE;
+    return launch_combine(L.p.O_part, L.p.LSE_part, B * Hq, Lq, num_splits, d, O, LSE, s);
+}
+
 int attn_prefill_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq,
                     int Hkv, int Lq, int Lk, int d, int causal, float scale,
                     const float* alibi_slopes, int impl, void* stream) {

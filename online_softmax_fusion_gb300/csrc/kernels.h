@@ -42,6 +42,9 @@ struct PrefillParams {
     int window_right;         // >= 0: keys after i' + window_right are masked
     int pair_heads;           // tcgen05 kernel: a CTA's two Q tiles are two query
                               // heads of one KV group (1) or two row blocks (0)
+    int splits;               // > 1 (tcgen05 kernel): split-KV, grid z = split,
+    float* O_part;            //   fp32 partials [B, Hq, Lq, splits, d] instead of O
+    float* LSE_part;          //   and [B, Hq, Lq, splits] instead of LSE
     int* status;
 };
 

@@ -118,8 +118,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int head1 = pair_heads ? 2 * hb + 1 : hb;
     const int row00 = pair_heads ? rb * 128 : rb * 256;
     const int row01 = pair_heads ? rb * 128 : rb * 256 + 128;
-    const KvRange rg0 = kv_range_for(row00, p, CAUSAL);
-    const KvRange rg1 = kv_range_for(row01, p, CAUSAL);
+    KvRange rg0 = kv_range_for(row00, p, CAUSAL);
+    KvRange rg1 = kv_range_for(row01, p, CAUSAL);
+    if (p.splits > 1) {
+        // split-KV: this CTA takes chunk blockIdx.z of the union of its two
+        // tiles' KV ranges and writes fp32 partials for a combine
+        const bool f0 = rg0.hi <= rg0.lo, f1 = rg1.hi <= rg1.lo;
+        if (!(f0 && f1)) {
+            const int ulo = f0 ? rg1.lo : (f1 ? rg0.lo : min(rg0.lo, rg1.lo));
+            const int uhi = f0 ? rg1.hi : (f1 ? rg0.hi : max(rg0.hi, rg1.hi));
+            const int chunk = (uhi - ulo + p.splits - 1) / p.splits;
+            const int s0 = ulo + int(blockIdx.z) * chunk;
+            const int s1 = min(uhi, s0 + chunk);
+            rg0.lo = max(rg0.lo, s0);
+            rg0.hi = min(rg0.hi, s1);
+            rg1.lo = max(rg1.lo, s0);
+            rg1.hi = min(rg1.hi, s1);
+        }
+    }
     const int kvh = head0 / p.G;
     // the CTA streams the union of its tiles' KV ranges
     const bool e0 = rg0.hi <= rg0.lo, e1 = rg1.hi <= rg1.lo;
@@ -499,7 +515,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) rr[i] = 0u;
                 }
-                if (valid) {
+                if (valid && p.splits > 1) {
+                    // split-KV partial: O / l in fp32, [B, Hq, Lq, splits, D]
+                    float* prow = p.O_part +
+                                  ((((size_t(b) * p.Hq + head) * p.Lq + row) * p.splits) +
+                                   blockIdx.z) * D + c * 32;
+#pragma unroll
+                    for (int v4 = 0; v4 < 8; ++v4)
+                        *reinterpret_cast<float4*>(prow + v4 * 4) =
+                            make_float4(__uint_as_float(rr[v4 * 4 + 0]) * inv,
+                                        __uint_as_float(rr[v4 * 4 + 1]) * inv,
+                                        __uint_as_float(rr[v4 * 4 + 2]) * inv,
+                                        __uint_as_float(rr[v4 * 4 + 3]) * inv);
+                } else if (valid) {
 #pragma unroll
                     for (int v8 = 0; v8 < 4; ++v8) {
                         uint4 w;
@@ -515,9 +543,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
             }
-            if (valid && p.LSE)
-                p.LSE[(size_t(b) * p.Hq + head) * p.Lq + row] =
-                    l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+            const float lse_row = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+            if (valid && p.splits > 1)
+                p.LSE_part[((size_t(b) * p.Hq + head) * p.Lq + row) * p.splits + blockIdx.z] = lse_row;
+            else if (valid && p.LSE)
+                p.LSE[(size_t(b) * p.Hq + head) * p.Lq + row] = lse_row;
         }
         tc::fence_before_sync();
     }
@@ -559,7 +589,7 @@ int launch_tc_t(const PrefillLaunch& L, cudaStream_t stream) {
     const int n_hb = L.p.pair_heads ? L.p.Hq / 2 : L.p.Hq;
     const long long items = (long long)((L.p.Lq + rows_per_item - 1) / rows_per_item) * n_hb;
     if (items > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-    dim3 grid(unsigned(items), L.p.B);
+    dim3 grid(unsigned(items), L.p.B, unsigned(L.p.splits > 1 ? L.p.splits : 1));
     prefill_tc_kernel<D, CAUSAL, ALIBI, EXTRA><<<grid, kTcThreads, smem, stream>>>(L.tmQ, L.tmK, L.tmV,
                                                                            L.p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

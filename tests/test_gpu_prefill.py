@@ -201,3 +201,37 @@ def test_softcap_window_unsupported_on_register_tile_kernel(attn):
     q = torch.zeros(1, 1, 128, 128, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(attn.AttnError):
         attn.prefill(q, q, q, impl="mma_sync", softcap=10.0)
+
+
+# ------------------------------------------------------------ split-KV prefill
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,causal,alibi,splits", [
+    (1, 8, 2, 512, 512, True, True, 2),       # GQA + ALiBi, the short sweep shape
+    (1, 8, 2, 512, 512, True, True, 4),
+    (2, 4, 4, 300, 300, True, False, 3),      # ragged, MHA
+    (1, 4, 2, 100, 700, False, False, 5),     # Lq < Lk, non-causal
+    (1, 2, 2, 256, 256, True, False, 8),      # more splits than KV tiles: empty splits
+    (1, 2, 1, 384, 130, True, False, 2),      # Lq > Lk: rows that see no key
+])
+def test_prefill_splitkv(attn, B, Hq, Hkv, Lq, Lk, causal, alibi, splits):
+    d = 128
+    q = _rand((B, Hq, Lq, d), 31 + Lq)
+    k = _rand((B, Hkv, Lk, d), 32 + Lk)
+    v = _rand((B, Hkv, Lk, d), 33 + Lk)
+    slopes = W.alibi_slopes(Hq) if alibi else None
+    scale = d ** -0.5
+    sl = None if slopes is None else slopes.cuda()
+    O, L = attn.prefill_splitkv(q.cuda(), k.cuda(), v.cuda(), splits, causal=causal, scale=scale,
+                                alibi_slopes=sl)
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    Or, Lr = attention_ref(q, k, v, scale=scale, causal=causal, alibi_slopes=slopes)
+    assert_o_close(O, Or)
+    assert_lse_close(L, Lr)
+    # the unsplit kernel on the same inputs agrees far inside the tolerance
+    O1, L1 = attn.prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale,
+                          alibi_slopes=sl)
+    torch.cuda.synchronize()
+    assert (O.float() - O1.float()).abs().max().item() <= 2e-2
+    fin = torch.isfinite(L1)
+    assert torch.equal(fin, torch.isfinite(L))
+    assert (L[fin] - L1[fin]).abs().max().item() <= 1e-4 if fin.any() else True

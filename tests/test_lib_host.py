@@ -167,3 +167,16 @@ def test_rmsnorm_matmul_validation_before_launch(L):
     S = L.attn_rmsnorm_matmul_splits(16, 4096, 4096)
     assert S in (1, 2, 4, 8)
     assert L.attn_rmsnorm_matmul_splits(1, 64, 8) == 1   # one K step
+
+
+def test_prefill_splitkv_validation_before_launch(L):
+    def sk(S, ws=P, wsb=1 << 30, Q=P):
+        return L.attn_prefill_splitkv(Q, P, P, P, None, 1, 4, 2, 128, 128, 128, 1, 0.1, None, S,
+                                      ws, wsb, None)
+    assert sk(0) == 4 and sk(17) == 4
+    assert sk(2, ws=None) == 1
+    assert sk(2, Q=None) == 1
+    assert sk(2, wsb=16) == 4
+    assert sk(2, ws=MIS) == 7
+    assert L.attn_prefill_splitkv_workspace_bytes(1, 4, 128, 128, 2) == 4 * 128 * 2 * 129 * 4
+    assert L.attn_prefill_splitkv_workspace_bytes(1, 4, 128, 128, 1) == 0
