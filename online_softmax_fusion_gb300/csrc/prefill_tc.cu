@@ -38,8 +38,12 @@ namespace {
 constexpr int kTcThreads = 384;                 // 12 warps = 3 warpgroups
 constexpr int kSoftmaxWarp0 = 4;                // warps 4..7: tile 0, 8..11: tile 1
 // Register split (setmaxnreg, per warpgroup): launch 168 x 384 = 64512;
-// producer/MMA group 80 x 128 + two softmax groups 192 x 256 = 59392.
-constexpr int kRegsCtl = 80;
+// producer/MMA group 96 x 128 + two softmax groups 192 x 256 = 61440 for
+// head dim 128 without softcap / window; 80 x 128 (59392) for the other
+// variants. Chosen per variant from the compiler's spill report: each split
+// is the one without spills (or with the fewest) for its variant.
+template <int D, bool EXTRA>
+constexpr int regs_ctl() { return (D == 128 && !EXTRA) ? 96 : 80; }
 constexpr int kRegsSoftmax = 192;
 constexpr float kRescaleThreshold = 8.0f;       // log2 units: rescale when max grows > 2^8
 constexpr uint32_t kTileBytes = 128 * 128;      // one 128-row x 128-byte swizzled box
@@ -171,7 +175,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp < kSoftmaxWarp0) {
       // control warpgroup: TMA producer (warp 0) and MMA issuer (warp 1)
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(regs_ctl<D, EXTRA>()));
       if (warp == 0) {
         // ============================================== TMA producer
         if (lane == 0) {
