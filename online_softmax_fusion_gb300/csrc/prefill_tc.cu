@@ -39,11 +39,10 @@ constexpr int kTcThreads = 384;                 // 12 warps = 3 warpgroups
 constexpr int kSoftmaxWarp0 = 4;                // warps 4..7: tile 0, 8..11: tile 1
 // Register split (setmaxnreg, per warpgroup): launch 168 x 384 = 64512;
 // producer/MMA group 96 x 128 + two softmax groups 192 x 256 = 61440 for
-// head dim 128 without softcap / window; 80 x 128 (59392) for the other
-// variants. Chosen per variant from the compiler's spill report: each split
-// is the one without spills (or with the fewest) for its variant.
+// head dim 128, 80 x 128 (59392) for head dim 64: chosen from the
+// compiler's spill report (no spills in any variant).
 template <int D, bool EXTRA>
-constexpr int regs_ctl() { return (D == 128 && !EXTRA) ? 96 : 80; }
+constexpr int regs_ctl() { return D == 128 ? 96 : 80; }
 constexpr int kRegsSoftmax = 192;
 constexpr float kRescaleThreshold = 8.0f;       // log2 units: rescale when max grows > 2^8
 constexpr uint32_t kTileBytes = 128 * 128;      // one 128-row x 128-byte swizzled box
