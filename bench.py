@@ -659,16 +659,14 @@ def run_ours(args):
         hv = v.cpu().pin_memory()
         ho = torch.empty(O.shape, dtype=O.dtype).pin_memory()
         hl = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = attn.prefill_host_workspace(pc.B, pc.Hq, pc.Hkv, pc.Lq, pc.Lk, pc.d, dev)
         e2e_steps = max(3, min(args.steps, 10))
 
         def e2e_step():
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            attn.prefill(dq, dk, dv, causal=True, scale=pc.scale, out=O, lse=LSE)
-            ho.copy_(O, non_blocking=True)
-            hl.copy_(LSE, non_blocking=True)
+            # the library's host-buffer entry: chunked copies in, kernels,
+            # copies out, pipelined across streams
+            attn.prefill_host(hq, hk, hv, causal=True, scale=pc.scale, out=ho, lse=hl,
+                              workspace=ws, synchronize=False)
 
         e2e_step()
         torch.cuda.synchronize()
@@ -683,7 +681,7 @@ def run_ours(args):
         e2e = {"value": fl * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": (hq.numel() + hk.numel() + hv.numel()) * 2,
                "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4, "ms_per_step": e2e_ms}
-        del hq, hk, hv, ho, hl, dq, dk, dv
+        del hq, hk, hv, ho, hl, ws
 
     others = None
     if args.kernel == "all" and not args.no_other_workloads:

@@ -13,7 +13,8 @@
  *     a separate combine call that repairs them with the global max.
  *
  * Conventions for every entry point
- *   - All tensor pointers are DEVICE pointers of the current CUDA device.
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device,
+ *     except the host buffers of attn_prefill_host.
  *   - bf16 tensors are row-major and contiguous, innermost dimension last:
  *       Q [B, Hq, Lq, d]   K, V [B, Hkv, Lk, d]   O [B, Hq, Lq, d]
  *     LSE is fp32 [B, Hq, Lq] and holds the natural-log log-sum-exp of each
@@ -23,7 +24,9 @@
  *     multiple of Hkv.
  *   - Ownership: the caller allocates and owns every buffer. The library
  *     allocates no device or host memory, never frees, and never
- *     synchronises except inside attn_device_status().
+ *     synchronises except inside attn_device_status(). (attn_prefill_host
+ *     creates two copy streams and a ring of events per device on first
+ *     use and keeps them.)
  *   - Streams: every launch is asynchronous on the given stream
  *     (cudaStream_t passed as void*, NULL = legacy default stream).
  *   - Errors: arguments are validated before anything is launched; an
@@ -125,6 +128,44 @@ int attn_prefill_opts(const void* Q, const void* K, const void* V,
                       const attn_prefill_options* opts, void* stream);
 
 /*
+ * attn_prefill_host - attn_prefill_opts on HOST buffers, with the copies
+ * pipelined against the kernels. The problem is cut into chunks of KV-head
+ * units (one KV head and its Hq/Hkv query heads), contiguous in the
+ * [B, H, L, d] layouts; a chunk is either part of one batch item's heads or
+ * whole batch items. Per chunk: Q, K, V are copied host -> device on a copy
+ * stream of the library, the fused prefill runs on `stream` once they have
+ * landed, and O, LSE are copied device -> host on a second copy stream. The
+ * stages of consecutive chunks overlap.
+ *
+ *   Qh, Kh, Vh  bf16 host [B,Hq,Lq,d] / [B,Hkv,Lk,d]           (read)
+ *   Oh          bf16 host [B,Hq,Lq,d]                          (written)
+ *   LSEh        fp32 host [B,Hq,Lq], or NULL                   (written)
+ *               Page-locked host memory lets the copies overlap; with
+ *               pageable memory the result is the same, the copies are not
+ *               asynchronous.
+ *   opts        as attn_prefill_opts (alibi_slopes stays a DEVICE pointer).
+ *   chunk_kv_heads  KV-head units per chunk; <= 0: automatic (about 8
+ *               chunks); values above Hkv are rounded up to whole batch items.
+ *               attn_prefill_host_chunks() gives the resulting chunk count.
+ *   workspace   device, attn_prefill_host_workspace_bytes() bytes, 16-byte
+ *               aligned, owned by the caller: device copies of Q, K, V, O,
+ *               LSE (each region 256-byte aligned).
+ *
+ * Asynchronous: the call queues everything and returns; the host buffers
+ * must stay valid (and the inputs unchanged) until `stream` has passed this
+ * call, and O / LSE are complete once it has. Work queued on `stream` before
+ * the call finishes before the first copy starts; work queued after it starts
+ * after the last copy. Errors: as attn_prefill_opts, all checked before any
+ * copy is queued, plus ATTN_ERR_WORKSPACE for a short workspace.
+ */
+size_t attn_prefill_host_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int d);
+int attn_prefill_host_chunks(int B, int Hkv, int chunk_kv_heads);
+int attn_prefill_host(const void* Qh, const void* Kh, const void* Vh, void* Oh, float* LSEh,
+                      int B, int Hq, int Hkv, int Lq, int Lk, int d,
+                      const attn_prefill_options* opts, int chunk_kv_heads,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_backward - gradients of attn_prefill (causal / ALiBi / GQA variants).
  *
  * The single-pass backward the Twill review (xllm-io) describes in §七 7.2:
@@ -154,7 +195,7 @@ int attn_backward(const void* Q, const void* K, const void* V,
 /* attn_backward with the implementation chosen: ATTN_IMPL_TCGEN05 (head dim
  * 128 only: one CTA per 128-key block, the five products on tcgen05 with
  * S^T, dP^T, dQ^T, dV and dK in tensor memory, dQ added to the workspace
- * accumulator by TMA reduce-add), ATTN_IMPL_MMA_SYNC (register-tile form,
+ * accumulator with fp32 atomics), ATTN_IMPL_MMA_SYNC (register-tile form,
  * head dims 64 and 128, dQ added with atomics), or ATTN_IMPL_AUTO (tcgen05
  * for head dim 128, else mma.sync). ATTN_ERR_UNSUPPORTED for any other impl
  * or for tcgen05 with head dim 64. attn_backward is this with AUTO. */

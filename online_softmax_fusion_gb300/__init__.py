@@ -7,6 +7,7 @@ no fallback path.
 
 Entry points mirror include/attn.h:
     prefill(q, k, v, causal, scale, alibi_slopes, impl)  -> (O, LSE)
+    prefill_host(q, k, v, ...)  (host tensors, pipelined) -> (O, LSE)
     decode_splitk(q, k, v, kv_lens, scale, num_splits)   -> (O_part, LSE_part)
     combine(O_part, LSE_part)                            -> (O, LSE)
     decode(q, k, v, kv_lens, scale, num_splits)          -> (O, LSE)
@@ -44,6 +45,11 @@ SIGNATURES = {
                                                                    _c_void_p]),
     "attn_prefill_opts": (_c_int, [_c_void_p] * 5 + [_c_int] * 6 + [ctypes.POINTER(PrefillOptions),
                                                                      _c_void_p]),
+    "attn_prefill_host_workspace_bytes": (ctypes.c_size_t, [_c_int] * 6),
+    "attn_prefill_host_chunks": (_c_int, [_c_int] * 3),
+    "attn_prefill_host": (_c_int, [_c_void_p] * 5 + [_c_int] * 6 + [ctypes.POINTER(PrefillOptions),
+                                                                     _c_int, _c_void_p,
+                                                                     ctypes.c_size_t, _c_void_p]),
     "attn_prefill_splitkv_workspace_bytes": (ctypes.c_size_t, [_c_int] * 5),
     "attn_prefill_splitkv": (_c_int, [_c_void_p] * 5 + [_c_int] * 7 + [_c_float, _c_void_p, _c_int,
                                                                      _c_void_p, ctypes.c_size_t,
@@ -161,6 +167,67 @@ def prefill(q, k, v, causal=False, scale=None, alibi_slopes=None, impl="auto", o
                                    Lq, Lk, d, int(bool(causal)), float(scale), _ptr(alibi_slopes),
                                    IMPLS[impl], _stream())
     _check(st, "attn_prefill")
+    return out, lse
+
+
+def _req_host(t, name, dtype, dims):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype or t.dim() != dims or not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous {dtype} with {dims} dims")
+
+
+def prefill_host_workspace(B, Hq, Hkv, Lq, Lk, d, device=None):
+    """Device workspace for prefill_host (uint8 tensor of the required size)."""
+    n = lib().attn_prefill_host_workspace_bytes(B, Hq, Hkv, Lq, Lk, d)
+    if n == 0:
+        raise ValueError("invalid sizes")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def prefill_host(q, k, v, causal=False, scale=None, alibi_slopes=None, impl="auto",
+                 softcap=0.0, window=(-1, -1), chunk_kv_heads=0, out=None, lse=None,
+                 with_lse=True, workspace=None, synchronize=True):
+    """prefill on HOST tensors: q [B,Hq,Lq,d], k/v [B,Hkv,Lk,d] bf16 on the CPU
+    (page-locked for the copies to overlap the kernels). The library copies
+    chunks of KV heads in, runs the fused prefill per chunk on the current
+    stream and copies O / LSE back, the three stages pipelined. alibi_slopes is
+    a CUDA tensor. Returns (O, LSE or None) as CPU tensors; with
+    synchronize=False they are complete only once the current stream has
+    passed the call."""
+    _req_host(q, "q", torch.bfloat16, 4)
+    _req_host(k, "k", torch.bfloat16, 4)
+    _req_host(v, "v", torch.bfloat16, 4)
+    B, Hq, Lq, d = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k and v must be [B, Hkv, Lk, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if alibi_slopes is not None:
+        _req(alibi_slopes, "alibi_slopes", torch.float32, 1)
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin)
+    if lse is None and with_lse:
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, pin_memory=pin)
+    if out is not None:
+        _req_host(out, "out", torch.bfloat16, 4)
+    if lse is not None:
+        _req_host(lse, "lse", torch.float32, 3)
+    if workspace is None:
+        workspace = prefill_host_workspace(B, Hq, Hkv, Lq, Lk, d)
+    opts = PrefillOptions(int(bool(causal)), float(scale),
+                          None if alibi_slopes is None else alibi_slopes.data_ptr(),
+                          float(softcap), int(window[0]), int(window[1]), IMPLS[impl])
+    st = lib().attn_prefill_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Lq,
+                                 Lk, d, ctypes.byref(opts), int(chunk_kv_heads), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream())
+    _check(st, "attn_prefill_host")
+    if synchronize:
+        torch.cuda.current_stream().synchronize()
     return out, lse
 
 

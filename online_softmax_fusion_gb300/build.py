@@ -26,7 +26,7 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-r
               "-Xptxas", "-v", f"-I{INCLUDE}"]
 SOURCES = ["api.cu", "decode.cu", "prefill_mma.cu", "prefill_tc.cu", "decode_noalloc.cu",
            "backward.cu", "rmsnorm_matmul.cu",
-           "backward_tc.cu"]
+           "backward_tc.cu", "host_pipeline.cu"]
 
 
 def _nvcc() -> str:

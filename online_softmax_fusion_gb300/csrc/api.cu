@@ -80,22 +80,6 @@ int make_map(CUtensorMap* m, const void* base, int d, int L, long long outer, in
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-// fp32 tensor [outer, L, d] (d innermost, at most 256) as a 3-D tensor map
-// with a (d, box_rows, 1) box and no swizzle; the tcgen05 backward reduces
-// dQ tiles into it.
-int make_map_f32(CUtensorMap* m, const void* base, int d, int L, long long outer, int box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return ATTN_ERR_CUDA;
-    cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(L), cuuint64_t(outer)};
-    cuuint64_t strides[2] = {cuuint64_t(d) * 4, cuuint64_t(L) * cuuint64_t(d) * 4};
-    cuuint32_t box[3] = {cuuint32_t(d), cuuint32_t(box_rows), 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_common(int B, int Hq, int Hkv, int d, float scale) {
@@ -430,7 +414,6 @@ int attn_backward_ex(const void* Q, const void* K, const void* V, const void* O,
     if ((st = make_map(&L.tmdO, dO, d, Lq, (long long)B * Hq, 64))) return st;
     if ((st = make_map(&L.tmK, K, d, Lk, (long long)B * Hkv, 128))) return st;
     if ((st = make_map(&L.tmV, V, d, Lk, (long long)B * Hkv, 128))) return st;
-    if ((st = make_map_f32(&L.tmdQ, p.dQacc, d, Lq, (long long)B * Hq, 64))) return st;
     if ((st = launch_backward_prep(p, d, cs))) return st;
     if ((st = launch_backward_tc_main(L, cs))) return st;
     return launch_backward_convert(p, d, cs);

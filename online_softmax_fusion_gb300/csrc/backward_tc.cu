@@ -105,7 +105,7 @@ template <bool CAUSAL, bool ALIBI>
 __global__ void __launch_bounds__(kBtThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                  const __grid_constant__ CUtensorMap tmdQ, BwdParams p) {
+                  BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     BtSmem& sm = *reinterpret_cast<BtSmem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -164,7 +164,6 @@ __global__ void __launch_bounds__(kBtThreads, 1)
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             tma_prefetch_desc(&tmdO);
-            tma_prefetch_desc(&tmdQ);
             mbar_arrive_expect_tx(&sm.kv_full, 4 * kKVBox);
             const int zkv = b * p.Hkv + kvh;
             for (int bx = 0; bx < 2; ++bx) {
@@ -481,7 +480,7 @@ int launch_tc_t(const BwdTcLaunch& L, cudaStream_t stream) {
     const long long ctas = (long long)((L.p.Lk + kBtKeys - 1) / kBtKeys) * L.p.Hkv * L.p.B;
     if (ctas > 0x7fffffffLL) return ATTN_ERR_SHAPE;
     bwd_tc_kernel<CAUSAL, ALIBI><<<unsigned(ctas), kBtThreads, smem, stream>>>(
-        L.tmQ, L.tmK, L.tmV, L.tmdO, L.tmdQ, L.p);
+        L.tmQ, L.tmK, L.tmV, L.tmdO, L.p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

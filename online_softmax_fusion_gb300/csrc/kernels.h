@@ -78,7 +78,7 @@ int launch_backward_convert(const BwdParams& p, int d, cudaStream_t stream);
 // K / V maps with 128-row boxes (bf16, 128-byte swizzle), and the fp32 dQ
 // accumulator [B * Hq, Lq, 128] with a (128, 64) box, no swizzle.
 struct BwdTcLaunch {
-    CUtensorMap tmQ, tmK, tmV, tmdO, tmdQ;
+    CUtensorMap tmQ, tmK, tmV, tmdO;
     BwdParams p;
 };
 int launch_backward_tc_main(const BwdTcLaunch& L, cudaStream_t stream);

@@ -180,3 +180,56 @@ def test_prefill_splitkv_validation_before_launch(L):
     assert sk(2, ws=MIS) == 7
     assert L.attn_prefill_splitkv_workspace_bytes(1, 4, 128, 128, 2) == 4 * 128 * 2 * 129 * 4
     assert L.attn_prefill_splitkv_workspace_bytes(1, 4, 128, 128, 1) == 0
+
+
+def test_prefill_host_validation_before_copies(L):
+    """Host-buffer prefill: every invalid argument is rejected before any copy
+    or CUDA call (here no GPU exists, so reaching the device would give 5)."""
+    opts = attn.PrefillOptions(1, 0.1, None, 0.0, -1, -1, 0)
+    ws_need = L.attn_prefill_host_workspace_bytes(2, 8, 2, 100, 300, 128)
+    # Q, K, V, O regions (256-byte aligned) and LSE
+    rq = -(-2 * 8 * 100 * 128 * 2 // 256) * 256
+    rkv = -(-2 * 2 * 300 * 128 * 2 // 256) * 256
+    rl = -(-2 * 8 * 100 * 4 // 256) * 256
+    assert ws_need == 2 * rq + 2 * rkv + rl
+    assert L.attn_prefill_host_workspace_bytes(0, 8, 2, 100, 300, 128) == 0
+
+    def call(Qh=P, Oh=P, B=2, Hq=8, Hkv=2, Lq=100, Lk=300, d=128, o=opts, ws=P, wsb=ws_need):
+        return L.attn_prefill_host(Qh, P, P, Oh, None, B, Hq, Hkv, Lq, Lk, d,
+                                   None if o is None else ctypes.byref(o), 0, ws, wsb, None)
+    assert call(Qh=None) == 1
+    assert call(Oh=None) == 1
+    assert call(o=None) == 1
+    assert call(ws=None) == 1
+    assert call(Hq=6, Hkv=4) == 2
+    assert call(Lq=0) == 2
+    assert call(B=70000) == 2
+    assert call(d=96) == 3
+    assert call(o=attn.PrefillOptions(1, float("nan"), None, 0.0, -1, -1, 0)) == 8
+    assert call(o=attn.PrefillOptions(1, 0.1, None, -1.0, -1, -1, 0)) == 8
+    assert call(o=attn.PrefillOptions(1, 0.1, None, 0.0, -1, -1, 7)) == 3
+    assert call(ws=MIS) == 7
+    assert call(o=attn.PrefillOptions(1, 0.1, MIS.value, 0.0, -1, -1, 0)) == 7
+    assert call(wsb=ws_need - 1) == 4
+
+
+def test_prefill_host_chunking(L):
+    """Chunks are runs of KV-head units inside one batch item, or whole batch
+    items; automatic chunking aims at about 8 chunks."""
+    assert L.attn_prefill_host_chunks(4, 32, 0) == 8       # 16 KV heads per chunk
+    assert L.attn_prefill_host_chunks(4, 32, 8) == 16
+    assert L.attn_prefill_host_chunks(4, 32, 5) == 4 * 7   # ragged last chunk per item
+    assert L.attn_prefill_host_chunks(4, 32, 1) == 128
+    assert L.attn_prefill_host_chunks(4, 32, 33) == 2      # rounded up to 2 whole items
+    assert L.attn_prefill_host_chunks(5, 32, 64) == 3      # 2 + 2 + 1 items
+    assert L.attn_prefill_host_chunks(64, 8, 0) == 8       # 8 whole items per chunk
+    assert L.attn_prefill_host_chunks(1, 1, 0) == 1
+    assert L.attn_prefill_host_chunks(0, 8, 0) == 0
+
+
+def test_prefill_host_binding_rejects_device_tensors():
+    q = torch.zeros(1, 2, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        attn.prefill_host(q, q, q.float())
+    with pytest.raises(TypeError):
+        attn.prefill_host(None, q, q)
