@@ -410,8 +410,8 @@ int attn_backward_ex(const void* Q, const void* K, const void* V, const void* O,
     std::memset(&L, 0, sizeof(L));
     L.p = p;
     L.p.status = status_ptr();
-    if ((st = make_map(&L.tmQ, Q, d, Lq, (long long)B * Hq, 64))) return st;
-    if ((st = make_map(&L.tmdO, dO, d, Lq, (long long)B * Hq, 64))) return st;
+    if ((st = make_map(&L.tmQ, Q, d, Lq, (long long)B * Hq, 128))) return st;
+    if ((st = make_map(&L.tmdO, dO, d, Lq, (long long)B * Hq, 128))) return st;
     if ((st = make_map(&L.tmK, K, d, Lk, (long long)B * Hkv, 128))) return st;
     if ((st = make_map(&L.tmV, V, d, Lk, (long long)B * Hkv, 128))) return st;
     if ((st = launch_backward_prep(p, d, cs))) return st;
