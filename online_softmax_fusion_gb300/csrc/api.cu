@@ -103,9 +103,14 @@ int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
 //    ~100 KB (two per SM), less the epilogue's receive area when that gets
 //    its own space (small batch tiles; larger ones reuse the rings); the X
 //    ring takes a third (half for batch tiles >= 128) in 2..8 slots, a
-//    multiple of the converter groups, the W ring the rest (2..12 slots).
+//    multiple of the converter groups, the W ring the rest (2..12 slots);
+//  * converter warps: one thread per batch row and K step. A grid of one
+//    CTA per SM with batch tiles >= 128 launches 16 converter warps, so
+//    that two or more groups convert K steps at once (a single group's
+//    conversion, latency-bound, otherwise paces the loop); its X ring holds
+//    two slots per group and the W ring keeps at least 4.
 struct RmsGeometry {
-    int NB, w_stages, x_stages, splits, k_tiles, cvt_warps, cvt_groups, recv_separate;
+    int NB, w_stages, x_stages, splits, k_tiles, cvt_all, cvt_warps, cvt_groups, recv_separate;
 };
 
 RmsGeometry rms_geometry(int B, int H, int D, int splits_req, int tile_req) {
@@ -137,9 +142,17 @@ RmsGeometry rms_geometry(int B, int H, int D, int splits_req, int tile_req) {
     // converter warps per K step: one thread per batch row; the X ring gets a
     // third of the space (half for large batch tiles, whose X slots are big)
     g.cvt_warps = ceil_div(g.NB, 32);
-    const int x_share = g.NB >= 128 ? budget / 2 : budget / 3;
-    g.x_stages = std::max(2, std::min(kRmsMaxXStages, x_share / xslot));
-    g.cvt_groups = std::min(8 / g.cvt_warps, g.x_stages);
+    g.cvt_all = (base * g.splits <= sms && g.NB >= 128) ? 16 : 8;
+    if (g.cvt_all == 16) {
+        const int groups = 16 / g.cvt_warps;
+        const int fit = std::max(groups, (budget - 4 * wslot) / xslot);
+        g.x_stages = std::min({kRmsMaxXStages, 2 * groups, fit});
+        g.cvt_groups = std::min(groups, g.x_stages);
+    } else {
+        const int x_share = g.NB >= 128 ? budget / 2 : budget / 3;
+        g.x_stages = std::max(2, std::min(kRmsMaxXStages, x_share / xslot));
+        g.cvt_groups = std::min(8 / g.cvt_warps, g.x_stages);
+    }
     g.x_stages = std::max(g.cvt_groups, g.x_stages / g.cvt_groups * g.cvt_groups);
     g.w_stages = std::max(2, std::min(kRmsMaxWStages, (budget - g.x_stages * xslot) / wslot));
     while (!g.recv_separate && g.w_stages < kRmsMaxWStages &&
@@ -459,6 +472,7 @@ int attn_rmsnorm_matmul_tiled(const void* X, const void* G, const void* W, void*
     L.p.k_tiles = g.k_tiles;
     L.p.w_stages = g.w_stages;
     L.p.x_stages = g.x_stages;
+    L.p.cvt_all = g.cvt_all;
     L.p.cvt_warps = g.cvt_warps;
     L.p.cvt_groups = g.cvt_groups;
     L.p.recv_separate = g.recv_separate;

@@ -109,6 +109,7 @@ struct RmsParams {
     int k_tiles;                              // ceil(H / 64)
     int w_stages;                             // W ring depth
     int x_stages;                             // X ring depth
+    int cvt_all;                              // converter warps of the launch: 8 or 16
     int cvt_warps;                            // converter warps per K step (<= 8)
     int cvt_groups;                           // groups taking K steps in turn; divides x_stages
     int recv_separate;                        // the epilogue's receive area follows the rings

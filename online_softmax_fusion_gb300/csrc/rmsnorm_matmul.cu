@@ -50,9 +50,11 @@ namespace attn {
 
 namespace {
 
-constexpr int kRmThreads = 384;
-constexpr int kCvtWarp0 = 4;                  // warps 4..11 convert and finish
-constexpr int kCvtWarps = 8;
+constexpr int kCvtWarp0 = 4;                  // warps 4.. convert and finish
+// 8 converter warps (384 threads, two CTAs per SM) or 16 (640 threads, one
+// CTA per SM; large batch tiles convert two or more K steps at once)
+template <int CVT>
+constexpr int rm_threads() { return (kCvtWarp0 + CVT) * 32; }
 constexpr uint32_t kWBox = 64 * 128;          // 64 K rows x 64 features (128 B)
 constexpr uint32_t kWStageBytes = 2 * kWBox;  // 128 features
 constexpr int kEmptyExp = -1000;              // row exponent before any nonzero value
@@ -68,8 +70,8 @@ struct RmsSmem {
     uint32_t tmem_base;
     int abort;
     alignas(128) uint16_t gbuf[kRmsMaxXStages][64];  // G chunk of each X slot
-    int part_e[256];                  // per converter group: partial (E, s) per batch row
-    float part_s[256];
+    int part_e[512];                  // per converter group: partial (E, s) per batch row
+    float part_s[512];
     int row_e[256];                   // this CTA's partial (E, s) per batch row
     float row_s[256];
     float row_p[256];                 // 2^-E of the merged row
@@ -112,8 +114,9 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
 }
 
 // Barrier over the converter warps only (named barrier 1).
+template <int CVT>
 __device__ __forceinline__ void converter_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kCvtWarps * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(CVT * 32) : "memory");
 }
 
 // Largest |x| of 8 bf16 values, as the bit pattern of a non-negative bf16
@@ -153,7 +156,8 @@ __device__ __forceinline__ float sq2(uint32_t w, float sc, float acc) {
 // A converter group of cvt_warps = ceil(NB / 32) warps handles one K step
 // (one thread per batch row); cvt_groups groups take the K steps in turn, so
 // several steps are converted at once.
-__global__ void __launch_bounds__(kRmThreads, 2)
+template <int CVT>
+__global__ void __launch_bounds__(rm_threads<CVT>(), CVT == 8 ? 2 : 1)
     rmsnorm_matmul_kernel(const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmW, RmsParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -380,9 +384,9 @@ __global__ void __launch_bounds__(kRmThreads, 2)
                 sm.part_s[grp * NB + r] = Ssum;
             }
         }
-        converter_sync();
+        converter_sync<CVT>();
         // merge the groups (the split form of the repair, inside the CTA)
-        for (int r = cw * 32 + lane; r < NB; r += kCvtWarps * 32) {
+        for (int r = cw * 32 + lane; r < NB; r += CVT * 32) {
             int em = kEmptyExp;
             for (int q = 0; q < ngroups; ++q) em = max(em, sm.part_e[q * NB + r]);
             float ss = 0.f;
@@ -416,7 +420,7 @@ __global__ void __launch_bounds__(kRmThreads, 2)
     const uint32_t tile_bytes = uint32_t(NB) * 128u * 4u;           // [S][NB][wd] fp32
     const uint32_t e_off = tile_bytes;                               // [S][NB] int
     const uint32_t s_off = tile_bytes + uint32_t(S * NB) * 4u;       // [S][NB] fp32
-    if (warp >= kCvtWarp0 && ok) {
+    if (warp >= kCvtWarp0 && warp < kCvtWarp0 + 8 && ok) {
         const int q4 = warp & 3;                          // TMEM lanes 32 q4 ..
         const int half = (warp - kCvtWarp0) >> 2;         // column half
         const int n = q4 * 32 + lane;                     // output feature in the tile
@@ -432,7 +436,7 @@ __global__ void __launch_bounds__(kRmThreads, 2)
                 st_cluster_u32(dst + uint32_t((c0 + cc + j) * wd * 4), v[j]);
         }
     }
-    for (int idx = threadIdx.x; idx < S * NB; idx += kRmThreads) {
+    for (int idx = threadIdx.x; idx < S * NB; idx += rm_threads<CVT>()) {
         const int q = idx / NB, r = idx - (idx / NB) * NB;
         const uint32_t o = uint32_t((int(rank) * NB + r) * 4);
         const uint32_t base = map_rank(recv_a, uint32_t(q));
@@ -445,7 +449,7 @@ __global__ void __launch_bounds__(kRmThreads, 2)
     // ---- merge the per-row statistics of the cluster (local)
     const int* re = reinterpret_cast<const int*>(recv + e_off);
     const float* rs = reinterpret_cast<const float*>(recv + s_off);
-    for (int r = threadIdx.x; r < NB; r += kRmThreads) {
+    for (int r = threadIdx.x; r < NB; r += rm_threads<CVT>()) {
         int em = kEmptyExp;
         for (int q = 0; q < S; ++q) em = max(em, re[q * NB + r]);
         float ss = 0.f;
@@ -476,7 +480,7 @@ __global__ void __launch_bounds__(kRmThreads, 2)
         const int q4n = wd / 4;
         const int nlo = int(rank) * wd;
         const float* rt = reinterpret_cast<const float*>(recv);
-        for (int u = threadIdx.x; u < NB * q4n; u += kRmThreads) {
+        for (int u = threadIdx.x; u < NB * q4n; u += rm_threads<CVT>()) {
             const int r = u / q4n;
             const int nl = (u - r * q4n) * 4;
             float4 acc = *reinterpret_cast<const float4*>(rt + r * wd + nl);
@@ -531,24 +535,26 @@ size_t smem_bytes(const RmsParams& p) {
 
 // Raises the kernel's dynamic shared-memory limit on the current device to at
 // least `smem` (never lowers it).
+template <int CVT>
 bool ensure_smem_attr(int dev, size_t smem) {
     static size_t attr_set[kMaxDev] = {0};
     if (attr_set[dev] >= smem) return true;
-    if (cudaFuncSetAttribute(rmsnorm_matmul_kernel,
+    if (cudaFuncSetAttribute(rmsnorm_matmul_kernel<CVT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
         return false;
     attr_set[dev] = smem;
     return true;
 }
 
+template <int CVT>
 int launch_t(const RmsLaunch& L, int dev, cudaStream_t stream) {
     const RmsParams& p = L.p;
     const size_t smem = smem_bytes(p);
-    if (!ensure_smem_attr(dev, smem)) return ATTN_ERR_CUDA;
+    if (!ensure_smem_attr<CVT>(dev, smem)) return ATTN_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned((p.D + 127) / 128), unsigned((p.B + p.NB - 1) / p.NB),
                        unsigned(p.splits));
-    cfg.blockDim = dim3(kRmThreads);
+    cfg.blockDim = dim3(rm_threads<CVT>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -558,7 +564,7 @@ int launch_t(const RmsLaunch& L, int dev, cudaStream_t stream) {
     attr[0].val.clusterDim.z = unsigned(p.splits);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, rmsnorm_matmul_kernel, L.tmX, L.tmW, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, rmsnorm_matmul_kernel<CVT>, L.tmX, L.tmW, p) != cudaSuccess) {
         (void)cudaGetLastError();
         return ATTN_ERR_CUDA;
     }
@@ -570,7 +576,9 @@ int launch_t(const RmsLaunch& L, int dev, cudaStream_t stream) {
 int launch_rmsnorm_matmul(const RmsLaunch& L, cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return ATTN_ERR_CUDA;
-    return launch_t(L, dev, stream);
+    if (L.p.cvt_all == 16) return launch_t<16>(L, dev, stream);
+    if (L.p.cvt_all == 8) return launch_t<8>(L, dev, stream);
+    return ATTN_ERR_UNSUPPORTED;
 }
 
 }  // namespace attn
