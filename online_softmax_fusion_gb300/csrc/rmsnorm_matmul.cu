@@ -119,17 +119,6 @@ __device__ __forceinline__ void converter_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(CVT * 32) : "memory");
 }
 
-// Largest |x| of 8 bf16 values, as the bit pattern of a non-negative bf16
-// (non-negative bf16 patterns order like their values).
-__device__ __forceinline__ uint32_t max_abs_bits8(const uint4& v) {
-    const uint32_t w[4] = {v.x & 0x7fff7fffu, v.y & 0x7fff7fffu, v.z & 0x7fff7fffu,
-                           v.w & 0x7fff7fffu};
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0xffffu, w[i] >> 16));
-    return m;
-}
-
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
     __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a),
                                *reinterpret_cast<const __nv_bfloat162*>(&b));

@@ -69,32 +69,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_ab(int M, int N, int a_mn, int
     return idesc_bf16(M, N, b_mn) | (uint32_t(a_mn) << 15);
 }
 
-// D[tmem] (+)= A[smem] * B[smem], issued by one thread.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem], issued by one thread. A (M x K bf16) sits in
-// tensor memory with row i in lane i and two K elements per 32-bit column
-// (the lower K index in the low half).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Warp-wide forms: the whole warp executes them with warp-uniform operands
-// and one elected lane issues the instruction. Keeping the issuing loop
+// D[tmem] (+)= A[smem] * B[smem] (ss) and D[tmem] (+)= A[tmem] * B[smem]
+// (ts; A, M x K bf16, sits in tensor memory with row i in lane i and two K
+// elements per 32-bit column, the lower K index in the low half). The whole
+// warp executes them with warp-uniform operands and one elected lane issues
+// the instruction. Keeping the issuing loop
 // warp-uniform lets the descriptors stay in uniform registers, which keeps
 // the MMA issue rate at the tensor core's pace while other warps on the
 // same scheduler are busy.
@@ -120,20 +99,13 @@ __device__ __forceinline__ void mma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tme
         : "memory");
 }
 
+// Arrives (count 1) on `bar` once every tcgen05 operation the elected lane
+// issued before it has completed.
 __device__ __forceinline__ void commit_warp(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-// Arrives (count 1) on `bar` once every tcgen05 operation this thread issued
-// before it has completed.
-__device__ __forceinline__ void commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
         : "memory");
 }
