@@ -102,6 +102,32 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, status));
 }
 
+// ----------------------------------------------------- thread-block clusters
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// A shared::cta address mapped to the same offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// All threads of all CTAs of the cluster; release/acquire orders the shared
+// memory writes before it with the distributed reads after it.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 // 3-D tiled bulk-tensor load global -> shared, completion counted in bytes on
 // `bar`. The innermost coordinate x must be a multiple of 8 elements (16 B).

@@ -78,30 +78,6 @@ struct RmsSmem {
     float row_c[256];                 // 1 / sqrt(s / H + eps 2^-2E) of the merged row
 };
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// All threads of all CTAs of the cluster; release/acquire orders the shared
-// memory writes before it with the distributed reads after it.
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile(
-        "barrier.cluster.arrive.release.aligned;\n\t"
-        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
-}
-
 // Untiled bulk copy global -> shared (16-byte aligned, size a multiple of 16),
 // completion counted in bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,
