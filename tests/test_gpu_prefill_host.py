@@ -46,6 +46,8 @@ CASES = [
     (2, 8, 8, 96, 300, 64, True, True, 3),        # MHA, d = 64, ALiBi slope offsets 0, 3, 6
     (4, 16, 2, 64, 64, 128, True, True, 0),       # whole batch items per chunk, ALiBi
     (1, 1, 1, 1, 1, 128, True, False, 0),         # one query, one key
+    (1, 4, 2, 300, 150, 128, True, False, 1),     # Lq > Lk: leading rows see no key
+    (2, 8, 8, 257, 513, 64, False, True, 3),      # non-causal ALiBi, ragged lengths, d = 64
 ]
 
 
