@@ -222,6 +222,99 @@ class ClockSampler:
         return self.summarize(lines, t0, t1)
 
 
+class NvmlSampler:
+    """Samples the SM clock, the clock-event (throttle) reasons and the power
+    of one GPU through NVML (read-only queries, ctypes) every `period_s` in a
+    background thread, so that a timed region of a few milliseconds still
+    holds tens of samples. stop(t0, t1) keeps the samples taken inside
+    [t0, t1] (time.time() seconds)."""
+    SM_CLOCK = 1
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int, uuid: str | None = None, period_s: float = 0.0005):
+        import ctypes
+        self.ct = ctypes
+        self.period = period_s
+        self.samples = []
+        self.thread = None
+        self.stop_flag = False
+        self.ok = False
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            found = False
+            if uuid:
+                found = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+            if not found:
+                found = lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) == 0
+            if not found:
+                return
+            self.lib, self.h = lib, h
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint()
+            lib.nvmlDeviceGetMaxClockInfo(h, self.SM_CLOCK, ctypes.byref(mx))
+            self.max_mhz = float(mx.value)
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _sample(self):
+        ct = self.ct
+        clk, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        t = time.time()
+        self.lib.nvmlDeviceGetClockInfo(self.h, self.SM_CLOCK, ct.byref(clk))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw))
+        self.reasons_fn(self.h, ct.byref(rs))
+        self.samples.append((t, float(clk.value), pw.value / 1000.0, int(rs.value)))
+
+    def _run(self):
+        while not self.stop_flag:
+            self._sample()
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            import threading
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+        return self
+
+    @classmethod
+    def summarize(cls, samples, max_mhz, t0=None, t1=None):
+        inside = [s for s in samples if t0 is None or t0 <= s[0] <= t1]
+        sm = [s[1] for s in inside]
+        reasons = sorted({name for s in inside for bit, name in cls.REASON_BITS.items()
+                          if s[3] & bit})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max_mhz,
+                "reasons": reasons, "samples_in_region": len(inside), "samples": len(samples),
+                "power_w_max": max((s[2] for s in inside), default=None),
+                "sm_mhz_min": min(sm) if sm else None, "source": "nvml"}
+
+    def stop(self, t0=None, t1=None):
+        self.stop_flag = True
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        return self.summarize(self.samples, self.max_mhz, t0, t1)
+
+
+def start_clock_sampler(dev):
+    """NVML sampling when the library is there, nvidia-smi otherwise."""
+    import torch
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    s = NvmlSampler(dev.index, uuid)
+    if s.ok:
+        return s.start()
+    return ClockSampler(dev.index).start()
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -297,10 +390,42 @@ def graph_time(fn, reps, replays=5):
     return e0.elapsed_time(e1) / (replays * reps)
 
 
-def measure_other_workloads(attn, W, dev, peaks):
+def prefill_check_sample(name, q, k, v, O, LSE, heads, rows, G, scale, causal=True,
+                         slopes=None, softcap=0.0, window=(-1, -1)):
+    """Host copies of what the oracle needs to check some rows of some heads
+    of a prefill output: the heads' query rows, their K/V heads and the
+    kernel's O / LSE rows."""
+    import torch
+    idx = torch.as_tensor(rows, dtype=torch.int64, device=q.device)
+    items = []
+    for b, h in heads:
+        kv = h // G
+        items.append({"q": q[b, h].index_select(0, idx).cpu(), "k": k[b, kv].cpu(),
+                      "v": v[b, kv].cpu(), "O": O[b, h].index_select(0, idx).cpu(),
+                      "LSE": LSE[b, h].index_select(0, idx).cpu(),
+                      "slope": None if slopes is None else float(slopes[h])})
+    return {"workload": name, "kind": "prefill", "rows": list(rows), "Lq": int(q.shape[2]),
+            "items": items, "scale": scale, "causal": causal, "softcap": softcap,
+            "window": window}
+
+
+def decode_check_sample(name, q, k, v, lens, O, LSE, pairs, G, scale):
+    """Host copies for an oracle check of some (batch entry, KV head) groups
+    of a decode output."""
+    items = []
+    for b, kvh in pairs:
+        n = int(lens[b])
+        items.append({"q": q[b, kvh * G:(kvh + 1) * G].cpu(), "k": k[b, kvh, :n].cpu(),
+                      "v": v[b, kvh, :n].cpu(), "O": O[b, kvh * G:(kvh + 1) * G].cpu(),
+                      "LSE": LSE[b, kvh * G:(kvh + 1) * G].cpu()})
+    return {"workload": name, "kind": "decode", "items": items, "scale": scale}
+
+
+def measure_other_workloads(attn, W, dev, peaks, checks):
     """The remaining workloads, each timed on its own (inputs > L2 except the
     smallest sweep lengths, which are noted): the causal GQA + ALiBi prefill
-    sweep over L and the long-context outlier decode with 64 splits."""
+    sweep over L and the long-context outlier decode with 64 splits. A small
+    sample of each output is appended to `checks` for the oracle leg."""
     import torch
     stream = torch.cuda.current_stream()
     sweep = []
@@ -319,6 +444,10 @@ def measure_other_workloads(attn, W, dev, peaks):
         in_bytes = (inp["q"].numel() + inp["k"].numel() + inp["v"].numel()) * 2
         sweep.append({"L": L, "ms": ms, "tflops": tf, "frac": tf / peaks["bf16_tflops"],
                       "inputs_exceed_l2": in_bytes > 129e6, "timing": "cuda graph replay"})
+        rows = W.sample_rows(L, 24, 4, L).tolist()
+        checks.append(prefill_check_sample(cfg.name, inp["q"], inp["k"], inp["v"], O, LSE,
+                                           [(0, 0), (0, 31)], rows, cfg.Hq // cfg.Hkv,
+                                           cfg.scale, slopes=inp["alibi_slopes"].cpu()))
         del inp, O, LSE
     # SoftCap and a causal sliding window on the causal MHA workload
     pc = W.PREFILL_CONFIGS[PREFILL_WORKLOAD]
@@ -336,6 +465,10 @@ def measure_other_workloads(attn, W, dev, peaks):
         variants.append({"variant": name, "ms": ms, "tflops": tf,
                          "frac": tf / peaks["bf16_tflops"], "flops": fl,
                          "workload": PREFILL_WORKLOAD, "timing": "cuda graph replay"})
+        rows = W.sample_rows(pc.Lq, 24, 4, 7).tolist()
+        checks.append(prefill_check_sample(f"{PREFILL_WORKLOAD} {name}", pin["q"], pin["k"],
+                                           pin["v"], Ov, Lv, [(1, 5)], rows, 1, pc.scale,
+                                           softcap=cap, window=win))
     del pin, Ov, Lv
     # backward of the causal MHA workload (forward outputs as its inputs)
     pc = W.PREFILL_CONFIGS[PREFILL_WORKLOAD]
@@ -370,6 +503,9 @@ def measure_other_workloads(attn, W, dev, peaks):
     long_dec = {"workload": dc.name, "splits": S, "ms_decode": t_dec, "ms_combine": t_cmb,
                 "kv_gbs": gbs, "path_gbs": kvb / ((t_dec + t_cmb) * 1e-3) / 1e9,
                 "frac": gbs / peaks["hbm_gbs"], "kv_bytes": kvb}
+    checks.append(decode_check_sample(dc.name, din["q"], din["k"], din["v"],
+                                      din["kv_lens"].cpu().tolist(), Od, Ld, [(0, 0), (3, 7)],
+                                      dc.Hq // dc.Hkv, dc.scale))
     del din, Op, Lp, Od, Ld
     # fused RMSNorm + product at the LLaMA-2-7B shape (H = D = 4096): the calls
     # cycle through 5 copies of W (5 x 32 MB > L2), so each reads W from HBM
@@ -393,6 +529,8 @@ def measure_other_workloads(attn, W, dev, peaks):
                     "frac_bf16": tf / peaks["bf16_tflops"], "bytes": byts, "flops": fl,
                     "splits": attn.lib().attn_rmsnorm_matmul_splits(cfg.B, cfg.H, cfg.D),
                     "timing": "cuda graph replay, W rotated over 5 copies (> L2)"})
+        checks.append({"workload": name, "kind": "rmsnorm", "x": rin["x"][:3].cpu(),
+                       "g": rin["g"].cpu(), "w": rin["w"].cpu(), "O": Orm[:3].cpu()})
         del rin, wcopies, Orm
     return {"prefill_gqa_alibi_sweep": sweep, "decode_long_outlier": long_dec,
             "backward_causal_mha_4k": bwd, "rmsnorm_matmul": rms,
@@ -434,6 +572,148 @@ def oracle_prefill_sample(budget_s: float, seed: int = 0):
     return flops, dt, desc
 
 
+class ErrorStats:
+    """Max / mean absolute error of outputs against the oracle, per workload."""
+
+    def __init__(self):
+        self.acc = {}
+
+    def add(self, name, O, Or, L=None, Lr=None):
+        import numpy as np
+        o = np.asarray(O.float().numpy() if hasattr(O, "float") else O, dtype=np.float64)
+        e = np.abs(o - np.asarray(Or, dtype=np.float64))
+        a = self.acc.setdefault(name, {"o_max_abs": 0.0, "o_sum": 0.0, "o_n": 0,
+                                       "lse_max_abs": 0.0, "rows": 0, "empty_rows_exact": True})
+        a["o_max_abs"] = max(a["o_max_abs"], float(e.max(initial=0.0)))
+        a["o_sum"] += float(e.sum())
+        a["o_n"] += e.size
+        if L is not None:
+            lg = np.asarray(L.numpy() if hasattr(L, "numpy") else L, dtype=np.float64)
+            lr = np.asarray(Lr, dtype=np.float64)
+            fin = np.isfinite(lr)
+            if fin.any():
+                a["lse_max_abs"] = max(a["lse_max_abs"], float(np.abs(lg[fin] - lr[fin]).max()))
+            empty = np.isneginf(lr)
+            if empty.any():
+                a["empty_rows_exact"] &= bool(np.all(np.isneginf(lg[empty])) and
+                                              np.all(o[empty] == 0.0))
+            a["rows"] += lr.size
+
+    def summary(self):
+        out = {}
+        for name, a in self.acc.items():
+            out[name] = {"o_max_abs": a["o_max_abs"],
+                         "o_mean_abs": a["o_sum"] / max(1, a["o_n"]),
+                         "lse_max_abs": a["lse_max_abs"], "rows": a["rows"],
+                         "empty_rows_exact": a["empty_rows_exact"]}
+        return out
+
+
+def oracle_leg(budget_s, prefill_ctx, decode_ctx, checks, dec_budget_s):
+    """The CPU oracle beside the kernels, on the bench's own inputs: times it
+    on the prefill workload (whole heads, rows in chunks of 512 from the
+    longest down, until budget_s is spent) and on the decode workload ((batch
+    entry, KV head) groups in order until dec_budget_s), and compares every
+    row it computes with the kernels' output of the timed steps; then checks
+    the samples the other workloads left in `checks`, and the single-head
+    workload. Returns (cpu_baseline dict, per-workload error stats)."""
+    import torch
+    import online_softmax_fusion_gb300 as attn
+    import workloads as W
+    from oracle import attention_ref, decode_ref, rmsnorm_matmul_ref
+    errs = ErrorStats()
+    cpu = {"kind": "oracle", "cores": cpu_cores(), "unit": "TFLOP/s"}
+    if prefill_ctx is not None:
+        pc = prefill_ctx["cfg"]
+        q, k, v, O, LSE = (prefill_ctx[x] for x in ("q", "k", "v", "O", "LSE"))
+        heads = [(b, h) for h in range(pc.Hq) for b in range(pc.B)]
+        flops = nrows = 0
+        t_or = 0.0
+        for (b, h) in heads:
+            if t_or >= budget_s:
+                break
+            qh, kh, vh = q[b:b + 1, h:h + 1].cpu(), k[b:b + 1, h:h + 1].cpu(), v[b:b + 1, h:h + 1].cpu()
+            Oh, Lh = O[b, h].cpu(), LSE[b, h].cpu()
+            done = 0
+            while done < pc.Lq and t_or < budget_s:
+                hi = pc.Lq - done
+                lo = max(0, hi - 512)
+                rows = list(range(lo, hi))
+                t0 = time.perf_counter()
+                Or, Lr = attention_ref(qh, kh, vh, scale=pc.scale, causal=True, rows=rows)
+                t_or += time.perf_counter() - t0
+                errs.add(pc.name, Oh[lo:hi], Or[0, 0], Lh[lo:hi], Lr[0, 0])
+                flops += 4 * pc.d * sum(i + 1 for i in rows)
+                nrows += hi - lo
+                done += hi - lo
+        cpu.update({"value": flops / t_or / 1e12, "seconds": round(t_or, 2),
+                    "sample": f"{nrows} causal rows of {pc.name} (its own inputs), "
+                              f"{flops / 1e9:.0f} GFLOP, fp64 numpy"})
+    if decode_ctx is not None:
+        dc = decode_ctx["cfg"]
+        q, k, v, lens, O, LSE = (decode_ctx[x] for x in ("q", "k", "v", "lens", "O", "LSE"))
+        G = dc.Hq // dc.Hkv
+        kvb = 0
+        t_or = 0.0
+        groups = 0
+        for b in range(dc.B):
+            for kvh in range(dc.Hkv):
+                if t_or >= dec_budget_s:
+                    break
+                n = int(lens[b])
+                qg = q[b:b + 1, kvh * G:(kvh + 1) * G].cpu()
+                kg, vg = k[b:b + 1, kvh:kvh + 1, :n].cpu(), v[b:b + 1, kvh:kvh + 1, :n].cpu()
+                t0 = time.perf_counter()
+                Or, Lr = decode_ref(qg, kg, vg, [n], scale=dc.scale)
+                t_or += time.perf_counter() - t0
+                errs.add(dc.name, O[b, kvh * G:(kvh + 1) * G].cpu(), Or[0],
+                         LSE[b, kvh * G:(kvh + 1) * G].cpu(), Lr[0])
+                kvb += 2 * n * dc.d * 2
+                groups += 1
+        cpu.update({"decode_value": kvb / t_or / 1e9, "decode_unit": "GB/s",
+                    "decode_seconds": round(t_or, 2),
+                    "decode_sample": f"{groups} (batch, KV head) groups of {dc.name} (its own "
+                                     f"inputs), {kvb / 1e9:.2f} GB of K/V, fp64 numpy"})
+    # the single-head workload: tiny, run here in full
+    c1 = W.PREFILL_CONFIGS["single_head_noncausal"]
+    inp = W.make_prefill_inputs(c1, "cpu")
+    O1, L1 = attn.prefill(inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda(), causal=False,
+                          scale=c1.scale)
+    Or, Lr = attention_ref(inp["q"], inp["k"], inp["v"], scale=c1.scale)
+    errs.add(c1.name, O1.cpu(), Or, L1.cpu(), Lr)
+    for c in checks:
+        if c["kind"] == "prefill":
+            for it in c["items"]:
+                rows = c["rows"]
+                qfull = torch.zeros((1, 1, c["Lq"], it["q"].shape[-1]), dtype=it["q"].dtype)
+                qfull[0, 0, rows] = it["q"]
+                Or, Lr = attention_ref(qfull, it["k"][None, None], it["v"][None, None],
+                                       scale=c["scale"], causal=c["causal"],
+                                       alibi_slopes=None if it["slope"] is None
+                                       else torch.tensor([it["slope"]]),
+                                       rows=rows, softcap=c["softcap"],
+                                       window_left=c["window"][0], window_right=c["window"][1])
+                errs.add(c["workload"], it["O"], Or[0, 0], it["LSE"], Lr[0, 0])
+        elif c["kind"] == "decode":
+            for it in c["items"]:
+                n = it["k"].shape[0]
+                Or, Lr = decode_ref(it["q"][None], it["k"][None, None], it["v"][None, None], [n],
+                                    scale=c["scale"])
+                errs.add(c["workload"], it["O"], Or[0], it["LSE"], Lr[0])
+        elif c["kind"] == "rmsnorm":
+            ref = rmsnorm_matmul_ref(c["x"], c["g"], c["w"])
+            errs.add(c["workload"], c["O"], ref)
+    summ = errs.summary()
+    if summ:
+        cpu["err_o_max_abs"] = max(v["o_max_abs"] for k, v in summ.items()
+                                   if not k.startswith("rmsnorm"))
+        cpu["err_o_mean_abs_worst"] = max(v["o_mean_abs"] for k, v in summ.items()
+                                          if not k.startswith("rmsnorm"))
+        cpu["err_lse_max_abs"] = max(v["lse_max_abs"] for v in summ.values())
+        cpu["err_workloads"] = len(summ)
+    return cpu, summ
+
+
 def cpu_cores() -> int:
     for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
         if os.environ.get(var, "").isdigit():
@@ -442,7 +722,19 @@ def cpu_cores() -> int:
 
 
 # ---------------------------------------------------------- reference arm
+def bench_config(kernel, pc, dc, world):
+    """The workload description both arms print (identical for the same run)."""
+    workload = {"all": f"{pc.name} + {dc.name}", "prefill": pc.name, "decode": dc.name}[kernel]
+    return {"workload": workload,
+            "prefill": {"B": pc.B, "H": pc.Hq, "L": pc.Lq, "d": pc.d, "causal": True}
+            if kernel in ("all", "prefill") else None,
+            "decode": {"B": dc.B, "Hq": dc.Hq, "Hkv": dc.Hkv, "d": dc.d,
+                       "kv_len": [dc.len_lo, dc.len_hi]} if kernel in ("all", "decode") else None,
+            "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args):
+    import workloads as W
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
@@ -462,8 +754,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total_t / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": PREFILL_WORKLOAD, "B": 4, "H": 32, "L": 4096, "d": 128,
-                   "causal": True, "sample": desc},
+        "config": bench_config("all", W.PREFILL_CONFIGS[PREFILL_WORKLOAD],
+                               W.DECODE_CONFIGS[DECODE_WORKLOAD], world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -597,7 +889,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     assert attn.device_status() == 0, "device status after warm-up"
 
-    clocks = ClockSampler(dev.index).start()
+    clocks = start_clock_sampler(dev)
     time.sleep(0.5)   # let nvidia-smi start sampling before the region opens
     nl = len(launches)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(args.steps)]
@@ -684,15 +976,18 @@ def run_ours(args):
         del hq, hk, hv, ho, hl, ws
 
     others = None
+    checks = []
     if args.kernel == "all" and not args.no_other_workloads:
-        others = measure_other_workloads(attn, W, dev, peaks)
+        others = measure_other_workloads(attn, W, dev, peaks, checks)
 
     if rank == 0:
-        cpu = None
+        cpu = errors = None
         if world == 1 and not args.no_cpu_baseline:
-            cfl, cdt, cdesc = oracle_prefill_sample(args.cpu_budget)
-            cpu = {"value": cfl / cdt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
-                   "kind": "oracle", "sample": cdesc, "seconds": round(cdt, 2)}
+            pctx = {"cfg": pc, "q": q, "k": k, "v": v, "O": O, "LSE": LSE} if do_p else None
+            dctx = {"cfg": dc, "q": din["q"], "k": din["k"], "v": din["v"],
+                    "lens": kv_lens.cpu().tolist(), "O": Od, "LSE": Ld} if do_d else None
+            cpu, errors = oracle_leg(args.cpu_budget, pctx, dctx, checks,
+                                     args.cpu_budget / 3)
         pk_t = peaks["bf16_tflops"]
         roof = None
         if do_p:
@@ -703,30 +998,31 @@ def run_ours(args):
                     "peak_kind": f"{peak_src} bf16 burst",
                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                     "kernel": "prefill_tc_kernel", "ms_per_launch": per["prefill"]}
+            if do_d:
+                # the decode's own roofline (HBM-bound), as plain keys beside it
+                dr = decode_obj["roofline"]
+                roof.update({"decode_kernel": "decode_splitk_kernel",
+                             "decode_bound": "hbm", "decode_achieved_gbs": dr["achieved"],
+                             "decode_peak_gbs": dr["peak"], "decode_frac": dr["frac"],
+                             "decode_traffic": dr["traffic"],
+                             "decode_kv_bytes": kvb, "decode_ms_per_launch": per["decode"],
+                             "combine_ms_per_launch": per["combine"]})
         elif do_d:
             roof = decode_obj["roofline"]
-        workload = {"all": f"{PREFILL_WORKLOAD} + {dc.name}", "prefill": PREFILL_WORKLOAD,
-                    "decode": dc.name}[args.kernel]
         out = {
             "metric": METRIC, "value": value,
             "unit": "TFLOP/s" if do_p else "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": workload,
-                       "prefill": {"B": pc.B, "H": pc.Hq, "L": pc.Lq, "d": pc.d, "causal": True,
-                                   "flops_per_step": fl} if do_p else None,
-                       "decode": {"B": dc.B, "Hq": dc.Hq, "Hkv": dc.Hkv, "d": dc.d,
-                                  "kv_len": [dc.len_lo, dc.len_hi], "splits": S,
-                                  "kv_bytes_per_step": kvb} if do_d else None,
-                       "l2": "inputs larger than L2 (no flush)",
-                       "parallelism": f"replicas x{world}"},
+            "config": bench_config(args.kernel, pc, dc, world),
             "roofline": roof,
             "decode": decode_obj,
             "e2e": e2e,
             "gpu_launches": nl * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
+            "errors_vs_oracle": errors,
             "other_workloads": others,
         }
         print(json.dumps(out), flush=True)

@@ -35,6 +35,10 @@
  *     wait that exceeds its time limit records ATTN_ERR_TIMEOUT in a device
  *     status word and the kernel returns; attn_device_status() reads it.
  *   - Supported head dims: d in {64, 128}. Pointers must be 16-byte aligned.
+ *   - Device lifetime: the library looks up the device addresses of its own
+ *     __device__ variables (the status word, the no-alloc decode's array)
+ *     once per device and keeps them. Do not call it on a device again after
+ *     cudaDeviceReset of that device in the same process.
  */
 #ifndef ATTN_H
 #define ATTN_H
@@ -360,6 +364,10 @@ int attn_decode(const void* Q, const void* K, const void* V, const int* kv_lens,
  *   - All calls on a device share the array; calls whose kernels overlap on
  *     the GPU (unordered streams) race on it. Nothing in it needs clearing:
  *     each call writes every partial it reads.
+ *   - The looked-up address is kept for the life of the process. After
+ *     cudaDeviceReset on a device the array lives at a new address, so do not
+ *     call this entry point (nor any other of this library, whose status word
+ *     is looked up the same way) on that device again in the same process.
  */
 int attn_decode_noalloc(const void* Q, const void* K, const void* V, const int* kv_lens,
                         int B, int Hq, int Hkv, int Lk_max, int d, float scale,
@@ -379,6 +387,22 @@ int attn_device_status(void* stream);
  * kernels use. The kernel records ATTN_ERR_TIMEOUT in the device status word
  * and returns; the context stays usable. Returns the launch status. */
 int attn_selftest_wait_timeout(int limit_ms, void* stream);
+
+/* Self-test of failure detection inside the tcgen05 prefill kernel (no
+ * counterpart in the pages). Runs attn_prefill (tcgen05 implementation, no
+ * ALiBi) with two changes: every device wait has a time limit of limit_ms
+ * (1..10000), and the first CTA's K/V producer never fills ring entry
+ * skip_entry (entries are consumed in the order K_0, V_0, K_1, V_1, ...), so
+ * that CTA's MMA warp must give up waiting, record ATTN_ERR_TIMEOUT in the
+ * device status word and wind the CTA down: the other warps leave their
+ * waits, the copies already in flight land, the issued products complete
+ * and the tensor memory is freed before the kernel returns. The other CTAs
+ * run normally. Arguments as attn_prefill; returns the launch status. The
+ * skipped CTA's rows of O and LSE are left unwritten when the entry was one
+ * they needed. */
+int attn_selftest_prefill_abort(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
+                                float scale, int skip_entry, int limit_ms, void* stream);
 
 /* Library ABI version (major * 100 + minor). */
 int attn_version(void);

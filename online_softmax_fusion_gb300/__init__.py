@@ -79,6 +79,8 @@ SIGNATURES = {
     "attn_device_status": (_c_int, [_c_void_p]),
     "attn_version": (_c_int, []),
     "attn_selftest_wait_timeout": (_c_int, [_c_int, _c_void_p]),
+    "attn_selftest_prefill_abort": (_c_int, [_c_void_p] * 5 + [_c_int] * 7 + [_c_float, _c_int,
+                                                                            _c_int, _c_void_p]),
 }
 
 _lib = None
@@ -261,10 +263,11 @@ def prefill_splitkv(q, k, v, num_splits, causal=False, scale=None, alibi_slopes=
 
 
 def backward(q, k, v, o, lse, dout, causal=False, scale=None, alibi_slopes=None,
-             workspace=None, impl="auto"):
+             workspace=None, impl="auto", dq=None, dk=None, dv=None):
     """Gradients of prefill: returns (dQ, dK, dV) bf16; dK and dV are per KV
     head (summed over a GQA group). `lse` is the forward's fp32 LSE. impl:
-    "auto" (tcgen05 for head dim 128), "tcgen05" or "mma_sync"."""
+    "auto" (tcgen05 for head dim 128), "tcgen05" or "mma_sync". dq / dk / dv:
+    optional output tensors shaped like q / k / v."""
     for t, n in ((q, "q"), (o, "o"), (dout, "dout")):
         _req(t, n, torch.bfloat16, 4)
     _req(k, "k", torch.bfloat16, 4)
@@ -279,9 +282,13 @@ def backward(q, k, v, o, lse, dout, causal=False, scale=None, alibi_slopes=None,
     nbytes = lib().attn_backward_workspace_bytes(B, Hq, Lq, d)
     if workspace is None:
         workspace = torch.empty(nbytes // 4, dtype=torch.float32, device=q.device)
-    dq = torch.empty_like(q)
-    dk = torch.empty_like(k)
-    dv = torch.empty_like(v)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, ref, n in ((dq, q, "dq"), (dk, k, "dk"), (dv, v, "dv")):
+        _req(t, n, torch.bfloat16, 4)
+        if t.shape != ref.shape:
+            raise ValueError(f"{n} must be shaped like its input")
     st = lib().attn_backward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
                                 _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Lq, Lk, d,
                                 int(bool(causal)), float(scale), _ptr(alibi_slopes),
@@ -425,6 +432,29 @@ def selftest_wait_timeout(limit_ms: int = 100):
     """Runs the bounded-wait self-test kernel on the current stream; the
     device status word then reads ATTN_ERR_TIMEOUT (see device_status)."""
     _check(lib().attn_selftest_wait_timeout(int(limit_ms), _stream()), "attn_selftest_wait_timeout")
+
+
+def selftest_prefill_abort(q, k, v, skip_entry, limit_ms=100, causal=False, scale=None,
+                           out=None, lse=None):
+    """The tcgen05 prefill with the first CTA's K/V ring entry skip_entry never
+    filled and every wait limited to limit_ms: that CTA must record
+    ATTN_ERR_TIMEOUT and return (see device_status). Returns (O, LSE)."""
+    _req(q, "q", torch.bfloat16, 4)
+    _req(k, "k", torch.bfloat16, 4)
+    _req(v, "v", torch.bfloat16, 4)
+    B, Hq, Lq, d = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    st = lib().attn_selftest_prefill_abort(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq,
+                                           Hkv, Lq, Lk, d, int(bool(causal)), float(scale),
+                                           int(skip_entry), int(limit_ms), _stream())
+    _check(st, "attn_selftest_prefill_abort")
+    return out, lse
 
 
 def device_status() -> int:

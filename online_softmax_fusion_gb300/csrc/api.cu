@@ -226,7 +226,8 @@ namespace {
 int prefill_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq,
                  int Hkv, int Lq, int Lk, int d, int causal, float scale,
                  const float* alibi_slopes, float softcap, int window_left, int window_right,
-                 int impl, void* stream) {
+                 int impl, void* stream, int selftest_skip = 0,
+                 unsigned long long wait_ns = 0) {
     if (!Q || !K || !V || !O) return ATTN_ERR_NULL;
     int st = check_common(B, Hq, Hkv, d, scale);
     if (st) return st;
@@ -258,6 +259,8 @@ int prefill_impl(const void* Q, const void* K, const void* V, void* O, float* LS
     L.p.pair_heads = (L.p.G % 2 == 0) ? 1 : 0;
     L.p.status = status_ptr();
     if (!L.p.status) return ATTN_ERR_CUDA;
+    L.p.selftest_skip = selftest_skip;
+    L.p.wait_ns = wait_ns;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     const bool want_tc = impl == ATTN_IMPL_TCGEN05 || impl == ATTN_IMPL_AUTO;
@@ -357,6 +360,15 @@ int attn_prefill(const void* Q, const void* K, const void* V, void* O, float* LS
                  void* stream) {
     return attn_prefill_ex(Q, K, V, O, LSE, B, Hq, Hkv, Lq, Lk, d, causal, scale, alibi_slopes,
                            ATTN_IMPL_AUTO, stream);
+}
+
+int attn_selftest_prefill_abort(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
+                                float scale, int skip_entry, int limit_ms, void* stream) {
+    if (skip_entry < 0 || limit_ms <= 0 || limit_ms > 10000) return ATTN_ERR_VALUE;
+    return prefill_impl(Q, K, V, O, LSE, B, Hq, Hkv, Lq, Lk, d, causal, scale, nullptr, 0.f, -1,
+                        -1, ATTN_IMPL_TCGEN05, stream, skip_entry + 1,
+                        (unsigned long long)limit_ms * 1000000ull);
 }
 
 size_t attn_backward_workspace_bytes(int B, int Hq, int Lq, int d) {

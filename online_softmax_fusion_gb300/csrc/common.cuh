@@ -102,6 +102,13 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, status));
 }
 
+// mbar_wait_warp with the time limit given.
+__device__ __forceinline__ bool mbar_wait_warp_limit(uint64_t* bar, uint32_t parity,
+                                                     volatile int* abort, int* status,
+                                                     unsigned long long limit_ns) {
+    return __all_sync(0xffffffffu, mbar_wait_limit(bar, parity, abort, status, limit_ns));
+}
+
 // ----------------------------------------------------- thread-block clusters
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;

@@ -46,6 +46,10 @@ struct PrefillParams {
     float* O_part;            //   fp32 partials [B, Hq, Lq, splits, d] instead of O
     float* LSE_part;          //   and [B, Hq, Lq, splits] instead of LSE
     int* status;
+    unsigned long long wait_ns;   // tcgen05 kernel: time limit of every device wait
+                                  // (0 = the library default)
+    int selftest_skip;        // failure-detection self-test only (0 = off): the first
+                              // CTA's producer never fills K/V ring entry selftest_skip - 1
 };
 
 struct PrefillLaunch {

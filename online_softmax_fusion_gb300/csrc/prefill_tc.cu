@@ -170,7 +170,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::fence_after_sync();
     const uint32_t tbase = sm.tmem_base;
     volatile int* abort = &sm.abort;
-    int issued = 0;   // TMA loads issued (producer thread)
+    const unsigned long long wlim = p.wait_ns ? p.wait_ns : kWaitLimitNs;
+    int issued = 0;   // ring entries issued (producer thread)
+    // failure-detection self-test: the first CTA never fills this ring entry,
+    // so the MMA warp's wait on it must run out and the CTA must wind down
+    const int skip = (p.selftest_skip > 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
+                      blockIdx.z == 0) ? p.selftest_skip - 1 : -1;
 
     if (warp < kSoftmaxWarp0) {
       // control warpgroup: TMA producer (warp 0) and MMA issuer (warp 1)
@@ -191,8 +196,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // ring order = consumption order: K_0, V_0, K_1, V_1, ...
             for (int u = 0; u < 2 * n; ++u) {
                 const int slot = u % NS;
-                if (u >= NS && !mbar_wait(&sm.kv_empty[slot], ((u / NS) - 1) & 1, abort, p.status))
+                if (u >= NS &&
+                    !mbar_wait_limit(&sm.kv_empty[slot], ((u / NS) - 1) & 1, abort, p.status, wlim))
                     break;
+                if (u == skip) {
+                    issued = u + 1;
+                    continue;
+                }
                 mbar_arrive_expect_tx(&sm.kv_full[slot], Cfg::kSlotBytes);
                 const CUtensorMap* map = (u & 1) ? &tmV : &tmK;
 #pragma unroll
@@ -204,16 +214,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (warp == 1) {
         // ============================================== MMA issuer
-        // (the whole warp runs the loop; one elected lane issues)
+        // (the whole warp runs the loop; one elected lane issues). Every wait
+        // here is the warp-uniform form: all lanes get the same result, so an
+        // abort never leaves part of the warp at an elect.sync.
         {
             constexpr uint32_t idS = tc::idesc_bf16(128, 128, 0);
             constexpr uint32_t idO = tc::idesc_bf16(128, D, 1);
-            bool ok = mbar_wait(&sm.bar_q, 0, abort, p.status);
+            bool ok = mbar_wait_warp_limit(&sm.bar_q, 0, abort, p.status, wlim);
             tc::fence_after_sync();
             int u = 0;   // next ring entry to consume
             auto acquire = [&]() {
                 const int slot = u % NS;
-                if (!mbar_wait(&sm.kv_full[slot], (u / NS) & 1, abort, p.status)) return -1;
+                if (!mbar_wait_warp_limit(&sm.kv_full[slot], (u / NS) & 1, abort, p.status, wlim))
+                    return -1;
                 tc::fence_after_sync();
                 return slot;
             };
@@ -279,7 +292,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int t = 0; ok && t < 2; ++t) {
                     const bool active = j >= rg[t].lo && j < rg[t].hi;
                     if (active) {
-                        ok = mbar_wait(&sm.p_full[t], pf[t] & 1, abort, p.status);
+                        ok = mbar_wait_warp_limit(&sm.p_full[t], pf[t] & 1, abort, p.status, wlim);
                         if (!ok) break;
                         ++pf[t];
                         tc::fence_after_sync();
@@ -306,7 +319,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // every MMA this thread issued completes before the CTA ends
             tc::commit_warp(&sm.mma_fin);
             volatile int never = 0;
-            mbar_wait(&sm.mma_fin, 0, &never, p.status);
+            mbar_wait_limit(&sm.mma_fin, 0, &never, p.status, wlim);
         }
       }
     } else {
@@ -336,7 +349,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = true;
         for (int jt = 0; jt < ntile; ++jt) {
             const int j = rgt.lo + jt;
-            ok = mbar_wait(&sm.s_full[t], jt & 1, abort, p.status);
+            // warp-uniform wait: the TMEM load below is warp-collective
+            ok = mbar_wait_warp_limit(&sm.s_full[t], jt & 1, abort, p.status, wlim);
             if (!ok) break;
             tc::fence_after_sync();
             float s[128];
@@ -501,7 +515,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
         // ---------------------------------------------------- epilogue
         if (ok && ntile > 0) {
-            ok = mbar_wait(&sm.o_done[t], 0, abort, p.status);
+            ok = mbar_wait_warp_limit(&sm.o_done[t], 0, abort, p.status, wlim);
             tc::fence_after_sync();
         }
         if (ok && !*abort) {
@@ -560,11 +574,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0 && lane == 0 && *abort) {
         // let this CTA's copies in flight land before its shared memory is released
         volatile int never = 0;
-        mbar_wait(&sm.bar_q, 0, &never, p.status);
+        mbar_wait_limit(&sm.bar_q, 0, &never, p.status, wlim);
         for (int s = 0; s < NS; ++s) {
             int last = -1;
-            for (int u = s; u < issued; u += NS) last = u;
-            if (last >= 0) mbar_wait(&sm.kv_full[s], (last / NS) & 1, &never, p.status);
+            for (int u = s; u < issued; u += NS)
+                if (u != skip) last = u;   // a skipped entry has nothing in flight
+            if (last >= 0) mbar_wait_limit(&sm.kv_full[s], (last / NS) & 1, &never, p.status, wlim);
         }
     }
     if (warp == 1) {

@@ -144,3 +144,31 @@ def test_window_pairs_brute_force(Lq, Lk, left, right, causal):
     assert bench.window_pairs(Lq, Lk, left, right, causal) == n
     if left < 0 and right < 0 and causal:
         assert n == bench.causal_pairs(Lq, Lk)
+
+
+def test_nvml_summary_keeps_samples_inside_the_region():
+    import bench
+    samples = [(0.9, 1500.0, 300.0, 0x1), (1.0, 2070.0, 900.0, 0x0),
+               (1.1, 2000.0, 1000.0, 0x4), (1.2, 2070.0, 950.0, 0x0), (1.5, 1200.0, 200.0, 0x8)]
+    c = bench.NvmlSampler.summarize(samples, 2070.0, 1.0, 1.2)
+    assert c["samples_in_region"] == 3 and c["samples"] == 5
+    assert c["sm_mhz"] == 2070.0 and c["sm_mhz_min"] == 2000.0
+    assert c["reasons"] == ["sw_power_cap"]          # the hw_slowdown sample lies outside
+    assert c["power_w_max"] == 1000.0
+
+
+def test_error_stats_flag_nonzero_rows_that_see_no_key():
+    import numpy as np
+    import bench
+    e = bench.ErrorStats()
+    ref = np.zeros((3, 4))
+    lr = np.array([-np.inf, 0.5, 1.0])
+    got = ref.copy()
+    got[1] += 0.01
+    e.add("w", got, ref, lr + np.array([0.0, 2e-4, 0.0]), lr)
+    s = e.summary()["w"]
+    assert abs(s["o_max_abs"] - 0.01) < 1e-12 and abs(s["lse_max_abs"] - 2e-4) < 1e-12
+    assert s["empty_rows_exact"]
+    got[0, 2] = 1e-3
+    e.add("w", got, ref, lr, lr)
+    assert not e.summary()["w"]["empty_rows_exact"]

@@ -6,7 +6,7 @@ import torch
 
 import workloads as W
 from oracle import combine_ref, decode_ref, decode_split_partials_ref
-from tests.parity import assert_lse_close, assert_o_close, to64
+from tests.parity import assert_attention_close
 
 pytestmark = pytest.mark.gpu
 
@@ -50,12 +50,10 @@ def test_decode_small(attn, B, Hq, Hkv, Lmax, d, lens, S):
     # partials against the oracle's local reductions
     Opr, Lpr = decode_split_partials_ref(q, k, v, kv_lens, scale=scale, split_len=C,
                                          num_splits=Sres)
-    assert_o_close(Op, Opr, what="O_part")
-    assert_lse_close(Lp, Lpr, what="LSE_part")
+    assert_attention_close(Op, Lp, Opr, Lpr)
     # merged result against the unsplit oracle
     Or, Lr = decode_ref(q, k, v, kv_lens, scale=scale)
-    assert_o_close(O, Or)
-    assert_lse_close(L, Lr)
+    assert_attention_close(O, L, Or, Lr)
 
 
 def test_decode_padding_garbage_is_ignored(attn):
@@ -71,8 +69,7 @@ def test_decode_padding_garbage_is_ignored(attn):
     kg[0, :, 78] = 3e4
     O, L = attn.decode(q.cuda(), kg.cuda(), vg.cuda(), lens.cuda(), num_splits=2)
     Or, Lr = decode_ref(q, k, v, lens, scale=d ** -0.5)
-    assert_o_close(O, Or)
-    assert_lse_close(L, Lr)
+    assert_attention_close(O, L, Or, Lr)
 
 
 def test_combine_against_oracle_partials(attn):
@@ -87,36 +84,37 @@ def test_combine_against_oracle_partials(attn):
     O, L = attn.combine(torch.tensor(Op, dtype=torch.float32).cuda(),
                         torch.tensor(Lp, dtype=torch.float32).cuda())
     Or, Lr = combine_ref(Op.astype(np.float32), Lp.astype(np.float32))
-    assert_o_close(O, Or)
-    assert_lse_close(L, Lr)
+    assert_attention_close(O, L, Or, Lr)
     assert torch.all(O[1, 2] == 0)
 
 
-def _full_size_sampled(attn, cfg, pairs):
+def _full_size(attn, cfg):
+    """The full workload on the GPU, then every (batch entry, KV head) group of
+    query heads against the oracle (K/V brought to the host one batch entry at
+    a time)."""
     inp = W.make_decode_inputs(cfg, "cuda")
     q, k, v, lens = inp["q"], inp["k"], inp["v"], inp["kv_lens"]
     O, L = attn.decode(q, k, v, lens, scale=cfg.scale, num_splits=cfg.num_splits)
     torch.cuda.synchronize()
     assert attn.device_status() == 0
-    G = cfg.Hq // cfg.Hkv
-    lens_c = lens.cpu()
-    for b, kvh in pairs:
+    Oc, Lc, qc, lens_c = O.cpu(), L.cpu(), q.cpu(), lens.cpu()
+    for b in range(cfg.B):
         n = int(lens_c[b])
-        Or, Lr = decode_ref(q[b:b + 1, kvh * G:(kvh + 1) * G].cpu(),
-                            k[b:b + 1, kvh:kvh + 1, :n].cpu(), v[b:b + 1, kvh:kvh + 1, :n].cpu(),
-                            lens_c[b:b + 1], scale=cfg.scale)
-        assert_o_close(O[b, kvh * G:(kvh + 1) * G], Or[0], what=f"O[{b},{kvh}]")
-        assert_lse_close(L[b, kvh * G:(kvh + 1) * G], Lr[0], what=f"LSE[{b},{kvh}]")
-    return inp, O, L
+        kb, vb = k[b:b + 1, :, :n].cpu(), v[b:b + 1, :, :n].cpu()
+        Or, Lr = decode_ref(qc[b:b + 1], kb, vb, lens_c[b:b + 1], scale=cfg.scale)
+        assert_attention_close(Oc[b], Lc[b], Or[0], Lr[0], what=f"[b={b}]")
+    return inp
 
 
-def test_decode_varlen_full_size_sampled(attn):
-    cfg = W.DECODE_CONFIGS["decode_gqa_varlen"]
-    _full_size_sampled(attn, cfg, [(0, 0), (17, 3), (40, 7), (63, 5), (31, 1)])
+def test_decode_varlen_full_size(attn):
+    """Batch 64, 32 query / 8 KV heads, kv_len uniform in [1024, 32768]:
+    every batch entry and head against the oracle."""
+    _full_size(attn, W.DECODE_CONFIGS["decode_gqa_varlen"])
 
 
-def test_decode_long_outlier_full_size_sampled(attn):
-    cfg = W.DECODE_CONFIGS["decode_long_outlier"]
-    inp, O, L = _full_size_sampled(attn, cfg, [(0, 0), (1, 4), (3, 7)])
+def test_decode_long_outlier_full_size(attn):
+    """Batch 4, 64 query / 8 KV heads, L = 131072 with 1% of K rows x8, 64
+    splits: every batch entry and head against the oracle."""
+    inp = _full_size(attn, W.DECODE_CONFIGS["decode_long_outlier"])
     # the outlier rows really are there (x8 keys): scores reach well past N(0,1)
     assert float(inp["k"][0, 0].float().abs().max()) > 16.0

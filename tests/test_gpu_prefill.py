@@ -1,8 +1,10 @@
 """GPU parity of the prefill kernels against the fp64 oracle, through the C ABI.
 
-Small cases are compared element by element over every row; the full-size
-workloads (causal MHA at L = 4096, the causal GQA + ALiBi sweep) are compared
-on seeded samples of query rows, each of which the oracle computes exactly.
+Every case is compared element by element with the oracle: the small cases,
+the full causal MHA workload (every head and row) and the causal GQA + ALiBi
+sweep up to L = 8192 in full; at L >= 16384 every head is compared on a seeded
+sample of rows plus the first and last 128 (rows are independent, so each is
+an exact check of that row).
 """
 import numpy as np
 import pytest
@@ -10,7 +12,7 @@ import torch
 
 import workloads as W
 from oracle import attention_ref
-from tests.parity import assert_lse_close, assert_o_close
+from tests.parity import assert_attention_close
 
 pytestmark = pytest.mark.gpu
 
@@ -42,8 +44,7 @@ def _run_case(attn, impl, B, Hq, Hkv, Lq, Lk, d, causal, alibi, seed=0, scale=No
     torch.cuda.synchronize()
     assert attn.device_status() == 0
     Or, Lr = attention_ref(q, k, v, scale=scale, causal=causal, alibi_slopes=slopes)
-    assert_o_close(O, Or)
-    assert_lse_close(L, Lr)
+    assert_attention_close(O, L, Or, Lr)
     return O, L
 
 
@@ -54,8 +55,7 @@ def test_single_head_noncausal_config(attn, impl):
     O, L = attn.prefill(inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda(), causal=False,
                         scale=cfg.scale, impl=impl)
     Or, Lr = attention_ref(inp["q"], inp["k"], inp["v"], scale=cfg.scale)
-    assert_o_close(O, Or)
-    assert_lse_close(L, Lr)
+    assert_attention_close(O, L, Or, Lr)
 
 
 @pytest.mark.parametrize("impl", IMPLS)
@@ -101,40 +101,60 @@ def test_causal_masking_is_exact(attn, impl):
         assert torch.equal(La[:, :, :cut], Lb[:, :, :cut])
 
 
-def _sampled_check(attn, cfg, impl, heads, n_random, seed):
+def _full_size_check(attn, cfg, impls, rows=None):
+    """Runs each implementation on the full workload, then compares every
+    query head of every batch entry with the oracle: every row when rows is
+    None, else the given rows of every head (rows are independent, so each
+    compared row is an exact check of that row)."""
     inp = W.make_prefill_inputs(cfg, "cuda")
     q, k, v, slopes = inp["q"], inp["k"], inp["v"], inp["alibi_slopes"]
-    O, L = attn.prefill(q, k, v, causal=cfg.causal, scale=cfg.scale, alibi_slopes=slopes,
-                        impl=impl)
-    torch.cuda.synchronize()
-    assert attn.device_status() == 0
-    rows = W.sample_rows(cfg.Lq, n_random, 128, seed).numpy()
+    outs = {}
+    for impl in impls:
+        O, L = attn.prefill(q, k, v, causal=cfg.causal, scale=cfg.scale, alibi_slopes=slopes,
+                            impl=impl)
+        torch.cuda.synchronize()
+        assert attn.device_status() == 0
+        if rows is not None:
+            idx = torch.from_numpy(rows).cuda()
+            O, L = O.index_select(2, idx), L.index_select(2, idx)
+        outs[impl] = (O.cpu(), L.cpu())
+        del O, L
+    qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+    del q, k, v
     G = cfg.Hq // cfg.Hkv
     sl = None if slopes is None else slopes.cpu()
-    for (b, h) in heads:
-        kv = h // G
-        Or, Lr = attention_ref(q[b:b + 1, h:h + 1].cpu(), k[b:b + 1, kv:kv + 1].cpu(),
-                               v[b:b + 1, kv:kv + 1].cpu(), scale=cfg.scale, causal=cfg.causal,
-                               alibi_slopes=None if sl is None else sl[h:h + 1], rows=rows)
-        idx = torch.from_numpy(rows).cuda()
-        assert_o_close(O[b, h].index_select(0, idx), Or[0, 0], what=f"O[{b},{h}]")
-        assert_lse_close(L[b, h].index_select(0, idx), Lr[0, 0], what=f"LSE[{b},{h}]")
-    del q, k, v, O, L
+    worst = 0.0
+    for b in range(cfg.B):
+        for h in range(cfg.Hq):
+            kv = h // G
+            Or, Lr = attention_ref(qc[b:b + 1, h:h + 1], kc[b:b + 1, kv:kv + 1],
+                                   vc[b:b + 1, kv:kv + 1], scale=cfg.scale, causal=cfg.causal,
+                                   alibi_slopes=None if sl is None else sl[h:h + 1], rows=rows)
+            for impl, (O, L) in outs.items():
+                (mx, _), _ = assert_attention_close(O[b, h], L[b, h], Or[0, 0], Lr[0, 0],
+                                                    what=f"[{impl}, b={b}, h={h}]")
+                worst = max(worst, mx)
+    return worst
 
 
-@pytest.mark.parametrize("impl", IMPLS)
-def test_causal_mha_4k_full_size_sampled(attn, impl):
-    cfg = W.PREFILL_CONFIGS["prefill_mha_causal_4k"]
-    _sampled_check(attn, cfg, impl, heads=[(0, 0), (1, 7), (2, 31), (3, 16)], n_random=256,
-                   seed=11)
+def test_causal_mha_4k_full_size(attn):
+    """Causal MHA at B=4, H=32, L=4096: every head and every row, both
+    tensor-core paths, against the oracle."""
+    _full_size_check(attn, W.PREFILL_CONFIGS["prefill_mha_causal_4k"], IMPLS)
 
 
-@pytest.mark.parametrize("L", [512, 1024, 2048, 4096, 8192, 16384, 32768, 65536])
-def test_gqa_alibi_sweep_sampled(attn, L):
-    cfg = W.gqa_sweep_config(L)
-    heads = [(0, 0), (0, 13), (0, 31)] if L >= 16384 else [(0, 0), (0, 5), (0, 18), (0, 31)]
-    _sampled_check(attn, cfg, "auto", heads=heads, n_random=512 if L >= 16384 else 256,
-                   seed=L)
+@pytest.mark.parametrize("L", [512, 1024, 2048, 4096, 8192])
+def test_gqa_alibi_sweep_full(attn, L):
+    """Causal GQA + ALiBi sweep up to L = 8192: every head, every row."""
+    _full_size_check(attn, W.gqa_sweep_config(L), ["auto"])
+
+
+@pytest.mark.parametrize("L", [16384, 32768, 65536])
+def test_gqa_alibi_sweep_long_sampled(attn, L):
+    """L >= 16384: every head on a seeded sample of 512 rows plus the first
+    and last 128 rows."""
+    rows = W.sample_rows(L, 512, 128, L).numpy()
+    _full_size_check(attn, W.gqa_sweep_config(L), ["auto"], rows=rows)
 
 
 @pytest.mark.skipif("tcgen05" not in IMPLS, reason="single tensor-core path built")
@@ -173,8 +193,7 @@ def test_prefill_softcap_window(attn, B, Hq, Hkv, Lq, Lk, d, causal, alibi, soft
     assert attn.device_status() == 0
     Or, Lr = attention_ref(q, k, v, scale=scale, causal=causal, alibi_slopes=slopes,
                            softcap=softcap, window_left=window[0], window_right=window[1])
-    assert_o_close(O, Or)
-    assert_lse_close(L, Lr)
+    assert_attention_close(O, L, Or, Lr)
 
 
 def test_window_long_sequence_sampled(attn):
@@ -187,14 +206,14 @@ def test_window_long_sequence_sampled(attn):
     O, Ls = attn.prefill(q, k, v, causal=True, window=(w, -1))
     torch.cuda.synchronize()
     assert attn.device_status() == 0
-    rows = W.sample_rows(L, 256, 64, 5).numpy()
-    for h in (0, 3):
+    rows = W.sample_rows(L, 512, 128, 5).numpy()
+    idx = torch.from_numpy(rows).cuda()
+    for h in range(4):
         Or, Lr = attention_ref(q[:, h:h + 1].cpu(), k[:, h // 2:h // 2 + 1].cpu(),
                                v[:, h // 2:h // 2 + 1].cpu(), scale=d ** -0.5, causal=True,
                                rows=rows, window_left=w)
-        idx = torch.from_numpy(rows).cuda()
-        assert_o_close(O[0, h].index_select(0, idx), Or[0, 0])
-        assert_lse_close(Ls[0, h].index_select(0, idx), Lr[0, 0])
+        assert_attention_close(O[0, h].index_select(0, idx), Ls[0, h].index_select(0, idx),
+                               Or[0, 0], Lr[0, 0], what=f"[h={h}]")
 
 
 def test_softcap_window_unsupported_on_register_tile_kernel(attn):
@@ -225,8 +244,7 @@ def test_prefill_splitkv(attn, B, Hq, Hkv, Lq, Lk, causal, alibi, splits):
     torch.cuda.synchronize()
     assert attn.device_status() == 0
     Or, Lr = attention_ref(q, k, v, scale=scale, causal=causal, alibi_slopes=slopes)
-    assert_o_close(O, Or)
-    assert_lse_close(L, Lr)
+    assert_attention_close(O, L, Or, Lr)
     # the unsplit kernel on the same inputs agrees far inside the tolerance
     O1, L1 = attn.prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale,
                           alibi_slopes=sl)

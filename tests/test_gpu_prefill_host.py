@@ -11,7 +11,7 @@ import torch
 
 import workloads as W
 from oracle import attention_ref
-from tests.parity import assert_lse_close, assert_o_close
+from tests.parity import assert_attention_close
 
 pytestmark = pytest.mark.gpu
 
@@ -67,8 +67,7 @@ def test_host_prefill_equals_device_prefill(attn, B, Hq, Hkv, Lq, Lk, d, causal,
     assert torch.equal(O, Od)
     assert torch.equal(L, Ld)
     Or, Lr = attention_ref(q, k, v, scale=scale, causal=causal, alibi_slopes=slopes)
-    assert_o_close(O, Or)
-    assert_lse_close(L, Lr)
+    assert_attention_close(O, L, Or, Lr)
 
 
 def test_host_prefill_options_and_pageable_memory(attn):

@@ -375,6 +375,54 @@ def test_softcap_matches_sdpa_with_capped_scores():
     assert np.max(np.abs(o2 - o3)) < 1e-9 and np.max(np.abs(l2 - l3)) < 1e-9
 
 
+def test_softcap_order_against_alibi_and_masks_by_hand():
+    """SoftCap caps the scaled score first; the ALiBi bias is added to the
+    capped score (unscaled); then the causal and window masks apply. Worked
+    by hand on three keys with one-dimensional heads, where capping after the
+    bias, scaling the bias, or dropping the cap all give different numbers."""
+    s, cap, slope = 0.5, 2.0, 0.5
+    q = np.array([[4.0], [3.0], [2.0]])             # rows i = 0, 1, 2 (Lq = Lk = 3)
+    k = np.array([[3.0], [-1.0], [3.0]])
+    v = np.array([[1.0, -2.0], [4.0, 0.5], [-3.0, 2.0]])
+
+    def by_hand(i, keys):
+        xs = []
+        for j in keys:
+            y = s * float(q[i, 0]) * float(k[j, 0])        # scaled score
+            x = cap * math.tanh(y / cap)                     # capped
+            x -= slope * abs(i - j)                          # ALiBi, not scaled
+            xs.append(x)
+        m = max(xs)
+        w = [math.exp(x - m) for x in xs]
+        tot = sum(w)
+        o = sum((wj / tot) * v[j] for wj, j in zip(w, keys))
+        return o, m + math.log(tot)
+
+    o, lse = attend_head(q, np.arange(3), k, v, scale=s, causal=True, slope=slope, softcap=cap,
+                         Lq=3, Lk=3)
+    for i in range(3):
+        oh, lh = by_hand(i, list(range(i + 1)))           # causal: keys 0..i
+        assert np.max(np.abs(o[i] - oh)) < 1e-14
+        assert abs(lse[i] - lh) < 1e-14
+    # row 0 sees key 0 only: O = v_0, LSE = cap * tanh(s q k / cap)
+    assert np.max(np.abs(o[0] - v[0])) < 1e-15
+    assert abs(lse[0] - cap * math.tanh(s * 12.0 / cap)) < 1e-14
+    # a left window of one key drops key 0 from row 2
+    o, lse = attend_head(q, np.arange(3), k, v, scale=s, causal=True, slope=slope, softcap=cap,
+                         window_left=1, Lq=3, Lk=3)
+    oh, lh = by_hand(2, [1, 2])
+    assert np.max(np.abs(o[2] - oh)) < 1e-14 and abs(lse[2] - lh) < 1e-14
+    # the other orders are far from it on this data
+    o, lse = attend_head(q, np.arange(3), k, v, scale=s, causal=True, slope=slope, softcap=cap,
+                         Lq=3, Lk=3)
+    y = s * q[2, 0] * k[:, 0]
+    dist = np.array([2.0, 1.0, 0.0])
+    for x_alt in (cap * np.tanh((y - slope * dist) / cap),    # cap after the bias
+                  cap * np.tanh(y / cap) - s * slope * dist,  # bias scaled
+                  y - slope * dist):                          # no cap
+        assert abs(lse[2] - (x_alt.max() + math.log(np.exp(x_alt - x_alt.max()).sum()))) > 0.05
+
+
 def test_window_zero_selects_the_aligned_key():
     """Window 0 on both sides: row i' sees only key i', so O_i = v_{i'} and
     LSE = its scaled score."""

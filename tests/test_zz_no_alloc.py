@@ -12,7 +12,8 @@ import ctypes
 import pytest
 import torch
 
-from tests.parity import assert_lse_close, assert_o_close
+from oracle import decode_ref
+from tests.parity import assert_attention_close, assert_o_close
 
 pytestmark = pytest.mark.gpu
 
@@ -36,33 +37,44 @@ def _inputs(B, Hq, Hkv, Lmax, d, seed):
 
 
 def _call_noalloc(lib, q, k, v, lens, S, O, LSE):
-    """Straight through the C ABI with plain pointers."""
+    """Straight through the C ABI with plain pointers (LSE may be None)."""
     B, Hq, d = q.shape
     Hkv, Lmax = k.shape[1], k.shape[2]
     st = lib.attn_decode_noalloc(
         ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
         ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(lens.data_ptr()),
         B, Hq, Hkv, Lmax, d, d ** -0.5, S, ctypes.c_void_p(O.data_ptr()),
-        ctypes.c_void_p(LSE.data_ptr()),
+        None if LSE is None else ctypes.c_void_p(LSE.data_ptr()),
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     return st
 
 
-def test_noalloc_matches_workspace_decode_twice(attn):
+def test_noalloc_matches_workspace_decode_and_oracle(attn):
     lib = attn.lib()
-    # two calls in a row with different shapes and split counts; the second
-    # reuses the array the first one filled
-    for (B, Hq, Hkv, Lmax, d, S, seed) in [(8, 32, 8, 3000, 128, 0, 1),
-                                           (4, 64, 8, 9000, 128, 64, 2)]:
+    # calls in a row with different shapes, head dims and split counts; each
+    # reuses the array the one before it filled. The last one passes no LSE.
+    for (B, Hq, Hkv, Lmax, d, S, seed, want_lse) in [(8, 32, 8, 3000, 128, 0, 1, True),
+                                                     (4, 64, 8, 9000, 128, 64, 2, True),
+                                                     (3, 16, 2, 700, 64, 3, 5, True),
+                                                     (2, 8, 2, 1500, 64, 0, 6, False)]:
         q, k, v, lens = _inputs(B, Hq, Hkv, Lmax, d, seed)
-        O_ref, L_ref = attn.decode(q, k, v, lens, num_splits=S)
+        O_ws, L_ws = attn.decode(q, k, v, lens, num_splits=S)
         O = torch.full((B, Hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
-        LSE = torch.full((B, Hq), float("nan"), dtype=torch.float32, device="cuda")
+        LSE = torch.full((B, Hq), float("nan"), dtype=torch.float32, device="cuda") \
+            if want_lse else None
         assert _call_noalloc(lib, q, k, v, lens, S, O, LSE) == 0
         torch.cuda.synchronize()
         assert attn.device_status() == 0
-        assert_o_close(O, O_ref.float().cpu().double())
-        assert_lse_close(LSE, L_ref.cpu().double())
+        # the same partials and combine as the workspace decode: identical output
+        assert torch.equal(O, O_ws)
+        if want_lse:
+            assert torch.equal(LSE, L_ws)
+        # and the oracle
+        Or, Lr = decode_ref(q.cpu(), k.cpu(), v.cpu(), lens.cpu(), scale=d ** -0.5)
+        if want_lse:
+            assert_attention_close(O, LSE, Or, Lr)
+        else:
+            assert_o_close(O, Or, lse_ref=Lr)
 
 
 def test_noalloc_rejects_sizes_beyond_its_array(attn):
