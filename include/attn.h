@@ -64,8 +64,11 @@ typedef enum {
 /* Prefill implementations selectable through attn_prefill_ex. */
 enum {
     ATTN_IMPL_AUTO = 0,         /* the fastest built kernel for the shape    */
-    ATTN_IMPL_TCGEN05 = 1,      /* warp-specialised tcgen05/TMEM/TMA kernel  */
-    ATTN_IMPL_MMA_SYNC = 2      /* register-tile mma.sync kernel             */
+    ATTN_IMPL_TCGEN05 = 1,      /* warp-specialised tcgen05/TMEM/TMA kernel,
+                                   two Q tiles per CTA, one CTA per SM       */
+    ATTN_IMPL_MMA_SYNC = 2,     /* register-tile mma.sync kernel             */
+    ATTN_IMPL_TCGEN05_1TILE = 3 /* the tcgen05 kernel with one Q tile per
+                                   CTA and two CTAs per SM                   */
 };
 
 /*
@@ -389,20 +392,21 @@ int attn_device_status(void* stream);
 int attn_selftest_wait_timeout(int limit_ms, void* stream);
 
 /* Self-test of failure detection inside the tcgen05 prefill kernel (no
- * counterpart in the pages). Runs attn_prefill (tcgen05 implementation, no
- * ALiBi) with two changes: every device wait has a time limit of limit_ms
- * (1..10000), and the first CTA's K/V producer never fills ring entry
- * skip_entry (entries are consumed in the order K_0, V_0, K_1, V_1, ...), so
- * that CTA's MMA warp must give up waiting, record ATTN_ERR_TIMEOUT in the
- * device status word and wind the CTA down: the other warps leave their
- * waits, the copies already in flight land, the issued products complete
- * and the tensor memory is freed before the kernel returns. The other CTAs
- * run normally. Arguments as attn_prefill; returns the launch status. The
- * skipped CTA's rows of O and LSE are left unwritten when the entry was one
- * they needed. */
+ * counterpart in the pages). Runs attn_prefill (no ALiBi) with the tcgen05
+ * form impl (ATTN_IMPL_TCGEN05 or ATTN_IMPL_TCGEN05_1TILE) and two changes:
+ * every device wait has a time limit of limit_ms (1..10000), and the first
+ * CTA's K/V producer stops before ring entry skip_entry (entries are
+ * consumed in the order K_0, V_0, K_1, V_1, ...), so that CTA's MMA warp must
+ * give up waiting, record ATTN_ERR_TIMEOUT in the device status word and
+ * wind the CTA down: the other warps leave their waits, the copies already
+ * in flight land, the issued products complete and the tensor memory is
+ * freed before the kernel returns. The other CTAs run normally. Arguments as
+ * attn_prefill; returns the launch status. The first CTA's rows of O and LSE
+ * are left unwritten when it needed the missing entries. */
 int attn_selftest_prefill_abort(const void* Q, const void* K, const void* V, void* O, float* LSE,
                                 int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
-                                float scale, int skip_entry, int limit_ms, void* stream);
+                                float scale, int skip_entry, int limit_ms, int impl,
+                                void* stream);
 
 /* Library ABI version (major * 100 + minor). */
 int attn_version(void);

@@ -24,7 +24,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libattn.so")
 
 ATTN_OK = 0
-IMPLS = {"auto": 0, "tcgen05": 1, "mma_sync": 2}
+IMPLS = {"auto": 0, "tcgen05": 1, "mma_sync": 2, "tcgen05_1tile": 3}
 
 _c_void_p = ctypes.c_void_p
 _c_int = ctypes.c_int
@@ -80,7 +80,8 @@ SIGNATURES = {
     "attn_version": (_c_int, []),
     "attn_selftest_wait_timeout": (_c_int, [_c_int, _c_void_p]),
     "attn_selftest_prefill_abort": (_c_int, [_c_void_p] * 5 + [_c_int] * 7 + [_c_float, _c_int,
-                                                                            _c_int, _c_void_p]),
+                                                                            _c_int, _c_int,
+                                                                            _c_void_p]),
 }
 
 _lib = None
@@ -435,10 +436,11 @@ def selftest_wait_timeout(limit_ms: int = 100):
 
 
 def selftest_prefill_abort(q, k, v, skip_entry, limit_ms=100, causal=False, scale=None,
-                           out=None, lse=None):
-    """The tcgen05 prefill with the first CTA's K/V ring entry skip_entry never
-    filled and every wait limited to limit_ms: that CTA must record
-    ATTN_ERR_TIMEOUT and return (see device_status). Returns (O, LSE)."""
+                           out=None, lse=None, impl="tcgen05"):
+    """The tcgen05 prefill (impl "tcgen05" or "tcgen05_1tile") whose first
+    CTA's producer stops before K/V ring entry skip_entry, with every wait
+    limited to limit_ms: that CTA must record ATTN_ERR_TIMEOUT and return (see
+    device_status). Returns (O, LSE)."""
     _req(q, "q", torch.bfloat16, 4)
     _req(k, "k", torch.bfloat16, 4)
     _req(v, "v", torch.bfloat16, 4)
@@ -452,7 +454,8 @@ def selftest_prefill_abort(q, k, v, skip_entry, limit_ms=100, causal=False, scal
         lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
     st = lib().attn_selftest_prefill_abort(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq,
                                            Hkv, Lq, Lk, d, int(bool(causal)), float(scale),
-                                           int(skip_entry), int(limit_ms), _stream())
+                                           int(skip_entry), int(limit_ms), IMPLS[impl],
+                                           _stream())
     _check(st, "attn_selftest_prefill_abort")
     return out, lse
 

@@ -24,7 +24,8 @@ INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-v", f"-I{INCLUDE}"]
-SOURCES = ["api.cu", "decode.cu", "prefill_mma.cu", "prefill_tc.cu", "decode_noalloc.cu",
+SOURCES = ["api.cu", "decode.cu", "prefill_mma.cu", "prefill_tc.cu", "prefill_tc1.cu",
+           "decode_noalloc.cu",
            "backward.cu", "rmsnorm_matmul.cu",
            "backward_tc.cu", "host_pipeline.cu"]
 

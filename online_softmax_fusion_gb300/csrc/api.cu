@@ -223,6 +223,23 @@ int attn_selftest_wait_timeout(int limit_ms, void* stream) {
 
 namespace {
 
+// Automatic choice between the two tcgen05 CTA forms (two Q tiles per CTA,
+// one CTA per SM; or one Q tile per CTA, two CTAs per SM), from measurements
+// on GB300: the one-tile form wins when the two-tile grid cannot fill the
+// SMs once (causal GQA + ALiBi at L = 512 and 1024: 1.2x and 1.14x), and
+// with SoftCap, whose softmax is bound by the special-function unit (two
+// CTAs per SM interleave it better, 1.06x); the two-tile form wins
+// everywhere else (L >= 2048: 1.08-1.1x).
+bool prefer_one_tile(const PrefillParams& p, int d) {
+    (void)d;
+    if (p.softcap > 0.f) return true;
+    const bool pair = p.pair_heads != 0;
+    const long long rows_per_item = pair ? 128 : 256;
+    const long long items = (p.Lq + rows_per_item - 1) / rows_per_item *
+                            (long long)(pair ? p.Hq / 2 : p.Hq) * p.B;
+    return items < sm_count();
+}
+
 int prefill_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq,
                  int Hkv, int Lq, int Lk, int d, int causal, float scale,
                  const float* alibi_slopes, float softcap, int window_left, int window_right,
@@ -236,7 +253,7 @@ int prefill_impl(const void* Q, const void* K, const void* V, void* O, float* LS
     if ((LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) ||
         (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)))
         return ATTN_ERR_ALIGN;
-    if (impl < ATTN_IMPL_AUTO || impl > ATTN_IMPL_MMA_SYNC) return ATTN_ERR_UNSUPPORTED;
+    if (impl < ATTN_IMPL_AUTO || impl > ATTN_IMPL_TCGEN05_1TILE) return ATTN_ERR_UNSUPPORTED;
     if (!std::isfinite(softcap) || softcap < 0.f) return ATTN_ERR_VALUE;
     const bool extra = softcap > 0.f || window_left >= 0 || window_right >= 0;
 
@@ -263,13 +280,16 @@ int prefill_impl(const void* Q, const void* K, const void* V, void* O, float* LS
     L.p.wait_ns = wait_ns;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    const bool want_tc = impl == ATTN_IMPL_TCGEN05 || impl == ATTN_IMPL_AUTO;
+    const bool want_tc = impl == ATTN_IMPL_TCGEN05 || impl == ATTN_IMPL_TCGEN05_1TILE ||
+                         impl == ATTN_IMPL_AUTO;
     if (want_tc) {
         if ((st = make_map(&L.tmQ, Q, d, Lq, (long long)B * Hq, kTcBM))) return st;
         if ((st = make_map(&L.tmK, K, d, Lk, (long long)B * Hkv, kTcBN))) return st;
         if ((st = make_map(&L.tmV, V, d, Lk, (long long)B * Hkv, kTcBN))) return st;
-        st = launch_prefill_tc(L, d, s);
-        if (st != ATTN_ERR_UNSUPPORTED || impl == ATTN_IMPL_TCGEN05) return st;
+        const bool one_tile = impl == ATTN_IMPL_TCGEN05_1TILE ||
+                              (impl == ATTN_IMPL_AUTO && prefer_one_tile(L.p, d));
+        st = one_tile ? launch_prefill_tc1(L, d, s) : launch_prefill_tc(L, d, s);
+        if (st != ATTN_ERR_UNSUPPORTED || impl != ATTN_IMPL_AUTO) return st;
     }
     // the register-tile kernel has no softcap / window variants
     if (extra) return ATTN_ERR_UNSUPPORTED;
@@ -364,10 +384,12 @@ int attn_prefill(const void* Q, const void* K, const void* V, void* O, float* LS
 
 int attn_selftest_prefill_abort(const void* Q, const void* K, const void* V, void* O, float* LSE,
                                 int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
-                                float scale, int skip_entry, int limit_ms, void* stream) {
+                                float scale, int skip_entry, int limit_ms, int impl,
+                                void* stream) {
     if (skip_entry < 0 || limit_ms <= 0 || limit_ms > 10000) return ATTN_ERR_VALUE;
+    if (impl != ATTN_IMPL_TCGEN05 && impl != ATTN_IMPL_TCGEN05_1TILE) return ATTN_ERR_UNSUPPORTED;
     return prefill_impl(Q, K, V, O, LSE, B, Hq, Hkv, Lq, Lk, d, causal, scale, nullptr, 0.f, -1,
-                        -1, ATTN_IMPL_TCGEN05, stream, skip_entry + 1,
+                        -1, impl, stream, skip_entry + 1,
                         (unsigned long long)limit_ms * 1000000ull);
 }
 

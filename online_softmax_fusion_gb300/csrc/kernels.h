@@ -49,7 +49,7 @@ struct PrefillParams {
     unsigned long long wait_ns;   // tcgen05 kernel: time limit of every device wait
                                   // (0 = the library default)
     int selftest_skip;        // failure-detection self-test only (0 = off): the first
-                              // CTA's producer never fills K/V ring entry selftest_skip - 1
+                              // CTA's producer stops before K/V ring entry selftest_skip - 1
 };
 
 struct PrefillLaunch {
@@ -100,7 +100,8 @@ int launch_prefill_mma(const PrefillLaunch& L, int d, cudaStream_t stream);
 // tcgen05 prefill: box rows for Q and K/V.
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 128;
-int launch_prefill_tc(const PrefillLaunch& L, int d, cudaStream_t stream);
+int launch_prefill_tc(const PrefillLaunch& L, int d, cudaStream_t stream);    // 2 Q tiles / CTA
+int launch_prefill_tc1(const PrefillLaunch& L, int d, cudaStream_t stream);   // 1 Q tile / CTA
 
 // Fused RMSNorm + matrix product: X [B, H], G [H], W [H, D] -> O [B, D].
 struct RmsParams {

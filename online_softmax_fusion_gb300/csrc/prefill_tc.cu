@@ -1,640 +1,11 @@
-// Warp-specialised tcgen05 prefill: the Rolling Update form of attention on
-// the 5th-generation tensor cores.
-//
-// Rolling Update (Neptune论文浅读 (gentlecold.top) §5) streams K/V tiles past
-// resident Q tiles and repairs the running sum and output with
-// exp(m_old - m_new) whenever the row max grows (§3-§4). The warp roles follow
-// the Blackwell schedule the Twill review (xllm-io) re-derives in §七 /
-// Figure 9: variable-latency loads in one warp, tensor-core GEMMs in another,
-// the softmax of two Q sub-tiles in two separate warp groups. That page puts
-// the accumulator rescaling in a third group because TMEM reads block; here
-// the rescale is conditional (it runs only when a row max grows by more than
-// 2^8, which after the first KV tile is rare) and the softmax group does it.
-//
-// CTA = two 128-row Q tiles that share one KV head: either two consecutive
-// row blocks of one head (MHA) or the same row block of two query heads of a
-// GQA group. Tensor memory (512 columns): S_0, S_1 (128 fp32 columns each),
-// O_0, O_1 (d columns each). P_t (bf16, two keys per column) is written over
-// the upper half of S_t, and the PV product reads it straight from tensor
-// memory, so per KV step shared memory only carries Q K^T's operands, V and
-// the TMA writes.
-//
-// Per KV step j, for each tile t (the two tiles alternate on the tensor core):
-//   TMA warp : K_j, V_j -> 5-slot shared-memory ring (128-byte swizzle)
-//   MMA warp : O_t += P_t V_j (A from TMEM), then S_t = Q_t K_{j+1}^T
-//   softmax t: S_t (TMEM) -> registers, row max, p = 2^(x - m), row sum,
-//              P_t (bf16) -> TMEM, O_t rescale in TMEM if needed
-// The commit that signals S_t^{j+1} also covers the PV product issued before
-// it, so when the softmax sees S_t^{j+1}, O_t is final for step j. One thread
-// owns one query row (TMEM lane = row): row reductions need no shuffles.
-#include "common.cuh"
-#include "kernels.h"
-#include "tcgen05.cuh"
+// The tcgen05 prefill with two Q tiles per CTA (one CTA per SM); the kernel
+// itself is in prefill_tc.cuh.
+#include "prefill_tc.cuh"
 
 namespace attn {
 
-namespace {
-
-constexpr int kTcThreads = 384;                 // 12 warps = 3 warpgroups
-constexpr int kSoftmaxWarp0 = 4;                // warps 4..7: tile 0, 8..11: tile 1
-// Register split (setmaxnreg, per warpgroup): launch 168 x 384 = 64512;
-// producer/MMA group 96 x 128 + two softmax groups 192 x 256 = 61440 for
-// head dim 128, 80 x 128 (59392) for head dim 64: chosen from the
-// compiler's spill report (no spills in any variant).
-template <int D, bool EXTRA>
-constexpr int regs_ctl() { return D == 128 ? 96 : 80; }
-constexpr int kRegsSoftmax = 192;
-constexpr float kRescaleThreshold = 8.0f;       // log2 units: rescale when max grows > 2^8
-constexpr uint32_t kTileBytes = 128 * 128;      // one 128-row x 128-byte swizzled box
-
-template <int D>
-struct TcCfg {
-    static constexpr int kBoxes = D / 64;                   // 64-element boxes per row
-    static constexpr int kStages = D == 128 ? 5 : 10;       // K/V ring slots
-    static constexpr uint32_t kSlotBytes = kBoxes * kTileBytes;
-};
-
-template <int D>
-struct TcSmem {
-    alignas(1024) uint8_t q[2][TcCfg<D>::kBoxes][kTileBytes];
-    alignas(1024) uint8_t kv[TcCfg<D>::kStages][TcCfg<D>::kBoxes][kTileBytes];
-    uint64_t bar_q;
-    uint64_t kv_full[TcCfg<D>::kStages];
-    uint64_t kv_empty[TcCfg<D>::kStages];
-    uint64_t s_full[2];
-    uint64_t p_full[2];
-    uint64_t o_done[2];
-    uint64_t mma_fin;
-    uint32_t tmem_base;
-    int abort;
-};
-
-// KV tiles [lo, hi) that the 128 query rows starting at row0 can see.
-struct KvRange {
-    int lo, hi;
-};
-
-__device__ __forceinline__ KvRange kv_range_for(int row0, const PrefillParams& p, bool causal) {
-    KvRange r{0, 0};
-    if (row0 >= p.Lq) return r;
-    const int off = p.Lk - p.Lq;
-    const int last = min(row0 + 127, p.Lq - 1);
-    int kend = p.Lk;
-    if (causal) kend = min(kend, last + off + 1);
-    if (p.window_right >= 0) kend = min(kend, last + off + p.window_right + 1);
-    int kbeg = 0;
-    if (p.window_left >= 0) kbeg = max(0, row0 + off - p.window_left);
-    if (kend <= kbeg) return r;
-    r.lo = kbeg / 128;
-    r.hi = (kend + 127) / 128;
-    return r;
-}
-
-}  // namespace
-
-// EXTRA: softcap and/or a sliding window is set (all tiles take the
-// per-element path).
-template <int D, bool CAUSAL, bool ALIBI, bool EXTRA>
-__global__ void __launch_bounds__(kTcThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
-                      const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, PrefillParams p) {
-    using Cfg = TcCfg<D>;
-    constexpr int NS = Cfg::kStages;
-    extern __shared__ uint8_t smem_raw[];
-    TcSmem<D>& sm = *reinterpret_cast<TcSmem<D>*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int b = blockIdx.y;
-    const int off = p.Lk - p.Lq;
-
-    // ---- work item: two Q tiles sharing one KV head, heaviest rows first
-    const int pair_heads = p.pair_heads;
-    const int n_hb = pair_heads ? p.Hq / 2 : p.Hq;
-    const int rows_per_item = pair_heads ? 128 : 256;
-    const int n_rb = (p.Lq + rows_per_item - 1) / rows_per_item;
-    const int rb = n_rb - 1 - int(blockIdx.x) / n_hb;
-    const int hb = int(blockIdx.x) % n_hb;
-    const int head0 = pair_heads ? 2 * hb : hb;
-    const int head1 = pair_heads ? 2 * hb + 1 : hb;
-    const int row00 = pair_heads ? rb * 128 : rb * 256;
-    const int row01 = pair_heads ? rb * 128 : rb * 256 + 128;
-    KvRange rg0 = kv_range_for(row00, p, CAUSAL);
-    KvRange rg1 = kv_range_for(row01, p, CAUSAL);
-    if (p.splits > 1) {
-        // split-KV: this CTA takes chunk blockIdx.z of the union of its two
-        // tiles' KV ranges and writes fp32 partials for a combine
-        const bool f0 = rg0.hi <= rg0.lo, f1 = rg1.hi <= rg1.lo;
-        if (!(f0 && f1)) {
-            const int ulo = f0 ? rg1.lo : (f1 ? rg0.lo : min(rg0.lo, rg1.lo));
-            const int uhi = f0 ? rg1.hi : (f1 ? rg0.hi : max(rg0.hi, rg1.hi));
-            const int chunk = (uhi - ulo + p.splits - 1) / p.splits;
-            const int s0 = ulo + int(blockIdx.z) * chunk;
-            const int s1 = min(uhi, s0 + chunk);
-            rg0.lo = max(rg0.lo, s0);
-            rg0.hi = min(rg0.hi, s1);
-            rg1.lo = max(rg1.lo, s0);
-            rg1.hi = min(rg1.hi, s1);
-        }
-    }
-    const int kvh = head0 / p.G;
-    // the CTA streams the union of its tiles' KV ranges
-    const bool e0 = rg0.hi <= rg0.lo, e1 = rg1.hi <= rg1.lo;
-    const int jlo = e0 ? rg1.lo : (e1 ? rg0.lo : min(rg0.lo, rg1.lo));
-    const int jhi = e0 ? rg1.hi : (e1 ? rg0.hi : max(rg0.hi, rg1.hi));
-    const int n = (e0 && e1) ? 0 : jhi - jlo;
-
-    if (threadIdx.x == 0) {
-        mbar_init(&sm.bar_q, 1);
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&sm.kv_full[i], 1);
-            mbar_init(&sm.kv_empty[i], 1);
-        }
-        for (int t = 0; t < 2; ++t) {
-            mbar_init(&sm.s_full[t], 1);
-            mbar_init(&sm.p_full[t], 4);
-            mbar_init(&sm.o_done[t], 1);
-        }
-        mbar_init(&sm.mma_fin, 1);
-        sm.abort = 0;
-        fence_mbar_init();
-    }
-    if (warp == 1) {
-        tc::tmem_alloc(&sm.tmem_base, 512);
-        tc::tmem_relinquish();
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tbase = sm.tmem_base;
-    volatile int* abort = &sm.abort;
-    const unsigned long long wlim = p.wait_ns ? p.wait_ns : kWaitLimitNs;
-    int issued = 0;   // ring entries issued (producer thread)
-    // failure-detection self-test: the first CTA never fills this ring entry,
-    // so the MMA warp's wait on it must run out and the CTA must wind down
-    const int skip = (p.selftest_skip > 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
-                      blockIdx.z == 0) ? p.selftest_skip - 1 : -1;
-
-    if (warp < kSoftmaxWarp0) {
-      // control warpgroup: TMA producer (warp 0) and MMA issuer (warp 1)
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(regs_ctl<D, EXTRA>()));
-      if (warp == 0) {
-        // ============================================== TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-            mbar_arrive_expect_tx(&sm.bar_q, 2u * Cfg::kBoxes * kTileBytes);
-#pragma unroll
-            for (int bx = 0; bx < Cfg::kBoxes; ++bx) {
-                tma_load_3d(sm.q[0][bx], &tmQ, &sm.bar_q, bx * 64, row00, b * p.Hq + head0);
-                tma_load_3d(sm.q[1][bx], &tmQ, &sm.bar_q, bx * 64, row01, b * p.Hq + head1);
-            }
-            const int z = b * p.Hkv + kvh;
-            // ring order = consumption order: K_0, V_0, K_1, V_1, ...
-            for (int u = 0; u < 2 * n; ++u) {
-                const int slot = u % NS;
-                if (u >= NS &&
-                    !mbar_wait_limit(&sm.kv_empty[slot], ((u / NS) - 1) & 1, abort, p.status, wlim))
-                    break;
-                if (u == skip) {
-                    issued = u + 1;
-                    continue;
-                }
-                mbar_arrive_expect_tx(&sm.kv_full[slot], Cfg::kSlotBytes);
-                const CUtensorMap* map = (u & 1) ? &tmV : &tmK;
-#pragma unroll
-                for (int bx = 0; bx < Cfg::kBoxes; ++bx)
-                    tma_load_3d(sm.kv[slot][bx], map, &sm.kv_full[slot], bx * 64,
-                                (jlo + (u >> 1)) * 128, z);
-                issued = u + 1;
-            }
-        }
-    } else if (warp == 1) {
-        // ============================================== MMA issuer
-        // (the whole warp runs the loop; one elected lane issues). Every wait
-        // here is the warp-uniform form: all lanes get the same result, so an
-        // abort never leaves part of the warp at an elect.sync.
-        {
-            constexpr uint32_t idS = tc::idesc_bf16(128, 128, 0);
-            constexpr uint32_t idO = tc::idesc_bf16(128, D, 1);
-            bool ok = mbar_wait_warp_limit(&sm.bar_q, 0, abort, p.status, wlim);
-            tc::fence_after_sync();
-            int u = 0;   // next ring entry to consume
-            auto acquire = [&]() {
-                const int slot = u % NS;
-                if (!mbar_wait_warp_limit(&sm.kv_full[slot], (u / NS) & 1, abort, p.status, wlim))
-                    return -1;
-                tc::fence_after_sync();
-                return slot;
-            };
-            auto release = [&](int slot) {
-                tc::commit_warp(&sm.kv_empty[slot]);
-                ++u;
-            };
-            // Descriptors are built once; a K-step or ring slot only moves the
-            // start-address field (16-byte units, 14 bits: every shared
-            // address here is below 256 KB, so the field cannot overflow).
-            const uint64_t qdesc0 = tc::sdesc_sw128(smem_u32(sm.q[0][0]), 16, 1024);
-            const uint64_t qdesc1 = tc::sdesc_sw128(smem_u32(sm.q[1][0]), 16, 1024);
-            const uint64_t kdesc0 = tc::sdesc_sw128(smem_u32(sm.kv[0][0]), 16, 1024);
-            const uint64_t vdesc0 = tc::sdesc_sw128(smem_u32(sm.kv[0][0]), kTileBytes, 1024);
-            constexpr uint32_t kSlotStep = Cfg::kSlotBytes >> 4;
-            auto issue_s = [&](int t, int slot) {
-                const uint64_t a0 = t ? qdesc1 : qdesc0;
-                const uint64_t b0 = kdesc0 + uint64_t(uint32_t(slot) * kSlotStep);
-                const uint32_t d = tbase + t * 128;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t o = ((kk >> 2) * kTileBytes + (kk & 3) * 32) >> 4;
-                    tc::mma_bf16_ss_warp(d, a0 + o, b0 + o, idS, kk > 0);
-                }
-            };
-            auto issue_pv = [&](int t, int slot, bool first) {
-                const uint64_t b0 = vdesc0 + uint64_t(uint32_t(slot) * kSlotStep);
-                const uint32_t tP = tbase + t * 128 + 64;
-                const uint32_t d = tbase + 256 + t * D;
-                const uint32_t acc0 = first ? 0u : 1u;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_bf16_ts_warp(d, tP + kk * 8, b0 + uint32_t(kk * (2048 >> 4)), idO,
-                                    kk > 0 ? 1u : acc0);
-            };
-            const KvRange rg[2] = {rg0, rg1};
-            int pf[2] = {0, 0};   // softmax steps consumed per tile (p_full phases)
-            if (ok && n > 0) {
-                const int ks = acquire();           // K_jlo
-                ok = ks >= 0;
-                if (ok) {
-                    for (int t = 0; t < 2; ++t)
-                        if (rg[t].lo == jlo && rg[t].hi > rg[t].lo) {
-                            issue_s(t, ks);
-                            tc::commit_warp(&sm.s_full[t]);
-                        }
-                    release(ks);
-                }
-            }
-            for (int jj = 0; ok && jj < n; ++jj) {
-                const int j = jlo + jj;
-                const int vs = acquire();           // V_j
-                if (vs < 0) break;
-                int ks = -1;
-                auto get_k = [&]() {                // K_{j+1} follows V_j in the ring
-                    if (ks < 0) {
-                        ++u;
-                        ks = acquire();
-                        --u;
-                    }
-                    return ks >= 0;
-                };
-                for (int t = 0; ok && t < 2; ++t) {
-                    const bool active = j >= rg[t].lo && j < rg[t].hi;
-                    if (active) {
-                        ok = mbar_wait_warp_limit(&sm.p_full[t], pf[t] & 1, abort, p.status, wlim);
-                        if (!ok) break;
-                        ++pf[t];
-                        tc::fence_after_sync();
-                        issue_pv(t, vs, j == rg[t].lo);
-                    }
-                    const bool next_s = (active && j + 1 < rg[t].hi) ||
-                                        (j + 1 == rg[t].lo && rg[t].hi > rg[t].lo);
-                    if (next_s) {
-                        if (!get_k()) { ok = false; break; }
-                        issue_s(t, ks);
-                        tc::commit_warp(&sm.s_full[t]);
-                    } else if (active) {
-                        tc::commit_warp(&sm.o_done[t]);
-                    }
-                }
-                if (!ok) break;
-                release(vs);
-                if (jj + 1 < n) {
-                    // every tile that needs K_{j+1} has consumed it by now
-                    if (!get_k()) break;
-                    release(ks);
-                }
-            }
-            // every MMA this thread issued completes before the CTA ends
-            tc::commit_warp(&sm.mma_fin);
-            volatile int never = 0;
-            mbar_wait_limit(&sm.mma_fin, 0, &never, p.status, wlim);
-        }
-      }
-    } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-        // ============================================== softmax groups
-        const int t = (warp - kSoftmaxWarp0) >> 2;
-        const int q4 = warp & 3;                  // TMEM lane quadrant of this warp
-        const int r = q4 * 32 + lane;             // row within the tile
-        const int head = t ? head1 : head0;
-        const int row0 = t ? row01 : row00;
-        const KvRange rgt = t ? rg1 : rg0;
-        const int ntile = rgt.hi > rgt.lo ? rgt.hi - rgt.lo : 0;
-        const int row = row0 + r;
-        const int i_al = row + off;               // bottom-right aligned row index
-        const uint32_t lane_off = uint32_t(q4 * 32) << 16;
-        const uint32_t tS = tbase + t * 128 + lane_off;
-        const uint32_t tP = tS + 64;
-        const uint32_t tO = tbase + 256 + t * D + lane_off;
-        const float sl2 = p.scale_log2;
-        // softcap in the natural-log domain: score / cap, then * cap * log2(e)
-        const float sc_div = EXTRA && p.softcap > 0.f ? (sl2 / kLog2e) / p.softcap : 0.f;
-        const float cap_l2 = EXTRA && p.softcap > 0.f ? p.softcap * kLog2e : 0.f;
-        const float slope_l2 = ALIBI ? p.slopes[head] * kLog2e : 0.f;
-
-        float m = -INFINITY;   // reference max (log2 domain)
-        float l = 0.f;
-        bool ok = true;
-        for (int jt = 0; jt < ntile; ++jt) {
-            const int j = rgt.lo + jt;
-            // warp-uniform wait: the TMEM load below is warp-collective
-            ok = mbar_wait_warp_limit(&sm.s_full[t], jt & 1, abort, p.status, wlim);
-            if (!ok) break;
-            tc::fence_after_sync();
-            float s[128];
-            {
-                uint32_t rr[128];
-                tc::tmem_ld_32x32b_x128(tS, rr);
-#pragma unroll
-                for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(rr[i]);
-            }
-            const int k0 = j * 128;
-            // aligned index of this warp's first row: the warp's 32 rows need
-            // per-key masks only on tiles that cross the key length, the
-            // causal diagonal or a window edge (warp-uniform)
-            const int w_al = row0 + q4 * 32 + off;
-            bool need_mask = (k0 + 128 > p.Lk) || (CAUSAL && k0 + 127 > w_al);
-            if (EXTRA) {
-                if (p.window_left >= 0 && k0 < w_al + 31 - p.window_left) need_mask = true;
-                if (p.window_right >= 0 && k0 + 127 > w_al + p.window_right) need_mask = true;
-            }
-            const bool cap = EXTRA && p.softcap > 0.f;
-            // x = s * scale (log2 domain) + bias, masked; on unmasked tiles
-            // without bias the scale is folded into the exp's FMA below
-            const bool fast = !need_mask && !ALIBI && !cap && sl2 > 0.f;
-            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            if (fast) {
-#pragma unroll
-                for (int c = 0; c < 128; c += 8) {
-                    mx4[0] = max3(mx4[0], s[c], s[c + 1]);
-                    mx4[1] = max3(mx4[1], s[c + 2], s[c + 3]);
-                    mx4[2] = max3(mx4[2], s[c + 4], s[c + 5]);
-                    mx4[3] = max3(mx4[3], s[c + 6], s[c + 7]);
-                }
-            } else if (ALIBI && CAUSAL && !need_mask && !cap) {
-                // every key of this tile is at or before every row of the
-                // warp: bias = slope * (key - i'), built from an exact integer
-                // counter c and one packed FMA per key pair, then fused into
-                // the scale: x = s * scale + slope * c + slope * (k0 - i')
-                const float b0 = slope_l2 * float(k0 - i_al);
-                const uint64_t slope2 = f2_pack(slope_l2, slope_l2);
-                const uint64_t b02 = f2_pack(b0, b0);
-                const uint64_t sc2 = f2_pack(sl2, sl2);
-                const uint64_t two2 = f2_pack(2.f, 2.f);
-                uint64_t cc2 = f2_pack(0.f, 1.f);
-#pragma unroll
-                for (int c = 0; c < 128; c += 2) {
-                    const uint64_t bias2 = f2_fma(cc2, slope2, b02);
-                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sc2, bias2), s[c], s[c + 1]);
-                    mx4[(c >> 1) & 3] = max3(mx4[(c >> 1) & 3], s[c], s[c + 1]);
-                    cc2 = f2_add(cc2, two2);
-                }
-            } else if (cap && !need_mask && !ALIBI) {
-                // unmasked tile with the cap: x = cap * tanh(score / cap), the
-                // same formula as the general path below without its masks
-#pragma unroll
-                for (int c = 0; c < 128; c += 2) {
-                    const float y0 = fminf(fmaxf(s[c] * sc_div, -15.f), 15.f);
-                    const float y1 = fminf(fmaxf(s[c + 1] * sc_div, -15.f), 15.f);
-                    const float e0 = ex2(y0 * (2.f * kLog2e));
-                    const float e1 = ex2(y1 * (2.f * kLog2e));
-                    s[c] = cap_l2 * ((e0 - 1.f) * rcp_approx(e0 + 1.f));
-                    s[c + 1] = cap_l2 * ((e1 - 1.f) * rcp_approx(e1 + 1.f));
-                    mx4[(c >> 1) & 3] = max3(mx4[(c >> 1) & 3], s[c], s[c + 1]);
-                }
-            } else {
-                // general tile: this row's visible keys form one interval
-                // [klo, khi] (key length, causal, window), computed once per
-                // tile; per key only the transform, the bias and one range test
-                int khi = p.Lk - 1;
-                if (CAUSAL) khi = min(khi, i_al);
-                int klo = 0;
-                if (EXTRA) {
-                    if (p.window_left >= 0) klo = max(klo, i_al - p.window_left);
-                    if (p.window_right >= 0) khi = min(khi, i_al + p.window_right);
-                }
-                const int clo = klo - k0, chi = khi - k0;
-                if (cap) {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        // cap * tanh(score / cap), tanh(y) = (e - 1) / (e + 1)
-                        // with e = 2^(2 y log2 e); |y| <= 15 keeps e finite
-                        // and tanh(15) rounds to 1 in fp32
-                        const float y = fminf(fmaxf(s[c] * sc_div, -15.f), 15.f);
-                        const float e = ex2(y * (2.f * kLog2e));
-                        float x = cap_l2 * ((e - 1.f) * rcp_approx(e + 1.f));
-                        if (ALIBI) {
-                            const float dist = float(i_al - (k0 + c));
-                            x -= slope_l2 * (CAUSAL ? dist : fabsf(dist));
-                        }
-                        if (c < clo || c > chi) x = -INFINITY;
-                        s[c] = x;
-                        mx4[c & 3] = fmaxf(mx4[c & 3], x);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        float x = s[c] * sl2;
-                        if (ALIBI) {
-                            const float dist = float(i_al - (k0 + c));
-                            x -= slope_l2 * (CAUSAL ? dist : fabsf(dist));
-                        }
-                        if (c < clo || c > chi) x = -INFINITY;
-                        s[c] = x;
-                        mx4[c & 3] = fmaxf(mx4[c & 3], x);
-                    }
-                }
-            }
-            float mx = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
-            if (fast) mx *= sl2;
-            // conditional repair: move the reference max only when the row max
-            // exceeds it by more than the threshold (or it is still unset)
-            float m_new = m;
-            if (mx > m + kRescaleThreshold || (m == -INFINITY && mx != -INFINITY)) m_new = mx;
-            const bool rescale = (jt > 0) && (m != -INFINITY) && (m_new != m);
-            const float corr = rescale ? ex2(m - m_new) : 1.f;
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            // p = 2^(x - m) as one packed FMA per key pair (x = s * scale on
-            // the fast path; s already holds x otherwise, times exactly 1),
-            // row sum with packed adds, and P_t (bf16) over the upper half of
-            // S_t in tensor memory, 64 keys at a time (S_t is in registers)
-            const float mul = fast ? sl2 : 1.f;
-            const uint64_t mul2 = f2_pack(mul, mul);
-            const uint64_t neg2 = f2_pack(-m_use, -m_use);
-            uint64_t sum2[2] = {0ull, 0ull};
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int c2 = 0; c2 < 32; ++c2) {
-                    const int c = h * 64 + 2 * c2;
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), mul2, neg2), x0, x1);
-                    const float p0 = ex2(x0);
-                    const float p1 = ex2(x1);
-                    sum2[c2 & 1] = f2_add(sum2[c2 & 1], f2_pack(p0, p1));
-                    pk[c2] = pack_bf16(p0, p1);
-                }
-                tc::tmem_st_32x32b_x32(tP + h * 32, pk);
-            }
-            float sa, sb, sc, sd;
-            f2_unpack(sum2[0], sa, sb);
-            f2_unpack(sum2[1], sc, sd);
-            l = l * corr + ((sa + sb) + (sc + sd));
-            m = m_new;
-            // O_t holds step j-1's result (the commit that signalled S_t^j
-            // covers the PV issued before it): repair it if the max moved
-            if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t rr[32];
-                    tc::tmem_ld_32x32b_x32(tO + c * 32, rr);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        rr[i] = __float_as_uint(__uint_as_float(rr[i]) * corr);
-                    tc::tmem_st_32x32b_x32(tO + c * 32, rr);
-                }
-            }
-            tc::tmem_wait_st();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.p_full[t]);
-        }
-
-        // ---------------------------------------------------- epilogue
-        if (ok && ntile > 0) {
-            ok = mbar_wait_warp_limit(&sm.o_done[t], 0, abort, p.status, wlim);
-            tc::fence_after_sync();
-        }
-        if (ok && !*abort) {
-            const bool valid = row < p.Lq;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16* orow =
-                p.O + ((size_t(b) * p.Hq + head) * p.Lq + (valid ? row : 0)) * D;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t rr[32];
-                if (ntile > 0) {
-                    tc::tmem_ld_32x32b_x32(tO + c * 32, rr);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) rr[i] = 0u;
-                }
-                if (valid && p.splits > 1) {
-                    // split-KV partial: O / l in fp32, [B, Hq, Lq, splits, D]
-                    float* prow = p.O_part +
-                                  ((((size_t(b) * p.Hq + head) * p.Lq + row) * p.splits) +
-                                   blockIdx.z) * D + c * 32;
-#pragma unroll
-                    for (int v4 = 0; v4 < 8; ++v4)
-                        *reinterpret_cast<float4*>(prow + v4 * 4) =
-                            make_float4(__uint_as_float(rr[v4 * 4 + 0]) * inv,
-                                        __uint_as_float(rr[v4 * 4 + 1]) * inv,
-                                        __uint_as_float(rr[v4 * 4 + 2]) * inv,
-                                        __uint_as_float(rr[v4 * 4 + 3]) * inv);
-                } else if (valid) {
-#pragma unroll
-                    for (int v8 = 0; v8 < 4; ++v8) {
-                        uint4 w;
-                        w.x = pack_bf16(__uint_as_float(rr[v8 * 8 + 0]) * inv,
-                                        __uint_as_float(rr[v8 * 8 + 1]) * inv);
-                        w.y = pack_bf16(__uint_as_float(rr[v8 * 8 + 2]) * inv,
-                                        __uint_as_float(rr[v8 * 8 + 3]) * inv);
-                        w.z = pack_bf16(__uint_as_float(rr[v8 * 8 + 4]) * inv,
-                                        __uint_as_float(rr[v8 * 8 + 5]) * inv);
-                        w.w = pack_bf16(__uint_as_float(rr[v8 * 8 + 6]) * inv,
-                                        __uint_as_float(rr[v8 * 8 + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + c * 32 + v8 * 8) = w;
-                    }
-                }
-            }
-            const float lse_row = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
-            if (valid && p.splits > 1)
-                p.LSE_part[((size_t(b) * p.Hq + head) * p.Lq + row) * p.splits + blockIdx.z] = lse_row;
-            else if (valid && p.LSE)
-                p.LSE[(size_t(b) * p.Hq + head) * p.Lq + row] = lse_row;
-        }
-        tc::fence_before_sync();
-    }
-
-    __syncwarp();
-    __syncthreads();
-    if (warp == 0 && lane == 0 && *abort) {
-        // let this CTA's copies in flight land before its shared memory is released
-        volatile int never = 0;
-        mbar_wait_limit(&sm.bar_q, 0, &never, p.status, wlim);
-        for (int s = 0; s < NS; ++s) {
-            int last = -1;
-            for (int u = s; u < issued; u += NS)
-                if (u != skip) last = u;   // a skipped entry has nothing in flight
-            if (last >= 0) mbar_wait_limit(&sm.kv_full[s], (last / NS) & 1, &never, p.status, wlim);
-        }
-    }
-    if (warp == 1) {
-        tc::fence_after_sync();
-        tc::tmem_dealloc(tbase, 512);
-    }
-}
-
-namespace {
-
-template <int D, bool CAUSAL, bool ALIBI, bool EXTRA>
-int launch_tc_t(const PrefillLaunch& L, cudaStream_t stream) {
-    const size_t smem = sizeof(TcSmem<D>) + 1024;
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(prefill_tc_kernel<D, CAUSAL, ALIBI, EXTRA>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(smem)) != cudaSuccess)
-            return ATTN_ERR_CUDA;
-        attr_set[dev] = true;
-    }
-    const int rows_per_item = L.p.pair_heads ? 128 : 256;
-    const int n_hb = L.p.pair_heads ? L.p.Hq / 2 : L.p.Hq;
-    const long long items = (long long)((L.p.Lq + rows_per_item - 1) / rows_per_item) * n_hb;
-    if (items > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-    dim3 grid(unsigned(items), L.p.B, unsigned(L.p.splits > 1 ? L.p.splits : 1));
-    prefill_tc_kernel<D, CAUSAL, ALIBI, EXTRA><<<grid, kTcThreads, smem, stream>>>(L.tmQ, L.tmK, L.tmV,
-                                                                           L.p);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
-}
-
-template <int D, bool EXTRA>
-int launch_tc_e(const PrefillLaunch& L, cudaStream_t stream) {
-    const bool alibi = L.p.slopes != nullptr;
-    if (L.p.causal)
-        return alibi ? launch_tc_t<D, true, true, EXTRA>(L, stream)
-                     : launch_tc_t<D, true, false, EXTRA>(L, stream);
-    return alibi ? launch_tc_t<D, false, true, EXTRA>(L, stream)
-                 : launch_tc_t<D, false, false, EXTRA>(L, stream);
-}
-
-template <int D>
-int launch_tc_d(const PrefillLaunch& L, cudaStream_t stream) {
-    const bool extra = L.p.softcap > 0.f || L.p.window_left >= 0 || L.p.window_right >= 0;
-    return extra ? launch_tc_e<D, true>(L, stream) : launch_tc_e<D, false>(L, stream);
-}
-
-}  // namespace
-
 int launch_prefill_tc(const PrefillLaunch& L, int d, cudaStream_t stream) {
-    if (d == 64) return launch_tc_d<64>(L, stream);
-    if (d == 128) return launch_tc_d<128>(L, stream);
-    return ATTN_ERR_UNSUPPORTED;
+    return launch_tc_nt<2>(L, d, stream);
 }
 
 }  // namespace attn

@@ -74,7 +74,7 @@ PREFILL_CASES = [
 ]
 
 
-@pytest.mark.parametrize("impl", ["tcgen05", "mma_sync"])
+@pytest.mark.parametrize("impl", ["tcgen05", "tcgen05_1tile", "mma_sync"])
 @pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,d,causal", PREFILL_CASES)
 def test_prefill_writes_exactly_its_output(attn, impl, B, Hq, Hkv, Lq, Lk, d, causal):
     q = _rand((B, Hq, Lq, d), Lq + 3 * Lk)

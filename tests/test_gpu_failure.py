@@ -43,15 +43,16 @@ def test_selftest_rejects_bad_limit(attn):
         attn.selftest_wait_timeout(0)
 
 
+@pytest.mark.parametrize("impl", ["tcgen05", "tcgen05_1tile"])
 @pytest.mark.parametrize("skip", [0, 3, 15])
-def test_prefill_kernel_abort_path(attn, skip):
-    """The real tcgen05 prefill with one K/V ring entry of its first CTA never
-    filled (entries K_0, V_0, K_1, ...; that CTA streams 8 KV tiles, so 15 is
-    its last entry) and a 100 ms limit on every wait. That CTA's MMA warp must
-    give up, record ATTN_ERR_TIMEOUT and wind the CTA down (warps leave their
-    waits together, copies in flight land, issued products complete, tensor
-    memory is freed); every other CTA's rows must be exact, and the next
-    ordinary prefill must match the oracle."""
+def test_prefill_kernel_abort_path(attn, skip, impl):
+    """The real tcgen05 prefill (both CTA forms) whose first CTA's producer
+    stops before one K/V ring entry (entries K_0, V_0, K_1, ...; that CTA
+    streams 8 KV tiles, so 15 is its last entry), with a 100 ms limit on every
+    wait. That CTA's MMA warp must give up, record ATTN_ERR_TIMEOUT and wind
+    the CTA down (warps leave their waits together, copies in flight land,
+    issued products complete, tensor memory is freed); every other CTA's rows
+    must be exact, and the next ordinary prefill must match the oracle."""
     from oracle import attention_ref
     from tests.parity import assert_attention_close
 
@@ -63,16 +64,19 @@ def test_prefill_kernel_abort_path(attn, skip):
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     assert attn.device_status() == 0
     t0 = time.time()
-    O, Ls = attn.selftest_prefill_abort(qd, kd, vd, skip, limit_ms=100, causal=True)
+    O, Ls = attn.selftest_prefill_abort(qd, kd, vd, skip, limit_ms=100, causal=True, impl=impl)
     st = attn.device_status()          # synchronises the stream
     dt = time.time() - t0
     assert st == ATTN_ERR_TIMEOUT
     assert 0.05 < dt < 5.0
     assert attn.device_status() == 0
     Or, Lr = attention_ref(q, k, v, scale=d ** -0.5, causal=True)
-    # the first CTA owns the heaviest row block (rows 768..1023) of head 0;
-    # every other row was computed by a CTA that ran normally
-    assert_attention_close(O[0, 0, :768], Ls[0, 0, :768], Or[0, 0, :768], Lr[0, 0, :768])
+    # the first CTA owns the heaviest row block of head 0 (rows 768..1023 with
+    # two tiles per CTA, 896..1023 with one); every other row was computed by
+    # a CTA that ran normally
+    first = 768 if impl == "tcgen05" else 896
+    assert_attention_close(O[0, 0, :first], Ls[0, 0, :first], Or[0, 0, :first],
+                           Lr[0, 0, :first])
     assert_attention_close(O[0, 1], Ls[0, 1], Or[0, 1], Lr[0, 1])
     # the context is intact: an ordinary prefill right after matches the oracle
     O2, L2 = attn.prefill(qd, kd, vd, causal=True)

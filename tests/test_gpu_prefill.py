@@ -16,7 +16,7 @@ from tests.parity import assert_attention_close
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = ["tcgen05", "mma_sync"]
+IMPLS = ["tcgen05", "tcgen05_1tile", "mma_sync"]
 
 
 @pytest.fixture(scope="module")
@@ -146,7 +146,7 @@ def test_causal_mha_4k_full_size(attn):
 @pytest.mark.parametrize("L", [512, 1024, 2048, 4096, 8192])
 def test_gqa_alibi_sweep_full(attn, L):
     """Causal GQA + ALiBi sweep up to L = 8192: every head, every row."""
-    _full_size_check(attn, W.gqa_sweep_config(L), ["auto"])
+    _full_size_check(attn, W.gqa_sweep_config(L), ["tcgen05", "tcgen05_1tile"])
 
 
 @pytest.mark.parametrize("L", [16384, 32768, 65536])
@@ -154,7 +154,7 @@ def test_gqa_alibi_sweep_long_sampled(attn, L):
     """L >= 16384: every head on a seeded sample of 512 rows plus the first
     and last 128 rows."""
     rows = W.sample_rows(L, 512, 128, L).numpy()
-    _full_size_check(attn, W.gqa_sweep_config(L), ["auto"], rows=rows)
+    _full_size_check(attn, W.gqa_sweep_config(L), ["tcgen05", "tcgen05_1tile"], rows=rows)
 
 
 @pytest.mark.skipif("tcgen05" not in IMPLS, reason="single tensor-core path built")
@@ -180,7 +180,9 @@ def test_impls_agree_closely(attn):
     (1, 2, 2, 100, 400, 128, True, False, 0.0, (50, -1)),      # Lq < Lk with window
     (1, 2, 2, 384, 384, 128, True, False, 0.0, (0, -1)),       # window 0: the diagonal only
 ])
-def test_prefill_softcap_window(attn, B, Hq, Hkv, Lq, Lk, d, causal, alibi, softcap, window):
+@pytest.mark.parametrize("impl", ["tcgen05", "tcgen05_1tile"])
+def test_prefill_softcap_window(attn, B, Hq, Hkv, Lq, Lk, d, causal, alibi, softcap, window,
+                                impl):
     q = _rand((B, Hq, Lq, d), Lq + 1, 2.0)
     k = _rand((B, Hkv, Lk, d), Lk + 2, 2.0)
     v = _rand((B, Hkv, Lk, d), Lk + 3)
@@ -188,7 +190,7 @@ def test_prefill_softcap_window(attn, B, Hq, Hkv, Lq, Lk, d, causal, alibi, soft
     scale = d ** -0.5
     O, L = attn.prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale,
                         alibi_slopes=None if slopes is None else slopes.cuda(),
-                        softcap=softcap, window=window)
+                        softcap=softcap, window=window, impl=impl)
     torch.cuda.synchronize()
     assert attn.device_status() == 0
     Or, Lr = attention_ref(q, k, v, scale=scale, causal=causal, alibi_slopes=slopes,
