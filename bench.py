@@ -516,10 +516,13 @@ def measure_other_workloads(attn, W, dev, peaks, checks):
         wcopies = [rin["w"]] + [rin["w"].clone() for _ in range(4)]
         Orm = torch.empty((cfg.B, cfg.D), dtype=torch.bfloat16, device=dev)
 
-        def fn_rms():
+        def fn_rms(chained):
             for wc in wcopies:
-                attn.rmsnorm_matmul(rin["x"], rin["g"], wc, out=Orm)
-        ms = graph_time(fn_rms, 4, replays=5) / len(wcopies)
+                attn.rmsnorm_matmul(rin["x"], rin["g"], wc, out=Orm, chained=chained)
+        ms_plain = graph_time(lambda: fn_rms(False), 4, replays=5) / len(wcopies)
+        # a stack of calls with constant weights: each launch overlaps the
+        # end of the one before (programmatic dependent launch)
+        ms = graph_time(lambda: fn_rms(True), 4, replays=5) / len(wcopies)
         byts = rmsnorm_matmul_bytes(cfg.B, cfg.H, cfg.D)
         fl = rmsnorm_matmul_flops(cfg.B, cfg.H, cfg.D)
         gbs = byts / (ms * 1e-3) / 1e9
@@ -528,7 +531,9 @@ def measure_other_workloads(attn, W, dev, peaks, checks):
                     "gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "tflops": tf,
                     "frac_bf16": tf / peaks["bf16_tflops"], "bytes": byts, "flops": fl,
                     "splits": attn.lib().attn_rmsnorm_matmul_splits(cfg.B, cfg.H, cfg.D),
-                    "timing": "cuda graph replay, W rotated over 5 copies (> L2)"})
+                    "ms_single_launch": ms_plain,
+                    "timing": "cuda graph replay of back-to-back chained calls, W rotated over "
+                              "5 copies (> L2); ms_single_launch: the same calls launched plainly"})
         checks.append({"workload": name, "kind": "rmsnorm", "x": rin["x"][:3].cpu(),
                        "g": rin["g"].cpu(), "w": rin["w"].cpu(), "O": Orm[:3].cpu()})
         del rin, wcopies, Orm

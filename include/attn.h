@@ -275,6 +275,26 @@ int attn_rmsnorm_matmul_tiled(const void* X, const void* G, const void* W, void*
                               int B, int H, int D, float eps, int batch_tile, int splits,
                               void* stream);
 
+/*
+ * attn_rmsnorm_matmul_chained - attn_rmsnorm_matmul for calls that follow one
+ * another on a stream with constant weights (no counterpart in the pages: a
+ * launch option of this library).
+ *
+ * The kernel is launched as a programmatic dependent of whatever kernel
+ * precedes it on the stream: it may start while that kernel is finishing,
+ * sets up and streams W at once, and waits for that kernel to complete
+ * before it reads X or G and before it writes O or RMS. Back-to-back calls
+ * (a stack of layers) thus overlap each call's start-up and first W tiles
+ * with the end of the call before.
+ *   Caller's promise: W is not written by the kernel that precedes this call
+ *   on the stream (it may still be running when W is read). X, G, O and RMS
+ *   carry no such restriction.
+ * Arguments, results and errors as attn_rmsnorm_matmul (automatic batch tile
+ * and K split).
+ */
+int attn_rmsnorm_matmul_chained(const void* X, const void* G, const void* W, void* O, float* rms,
+                                int B, int H, int D, float eps, void* stream);
+
 /* The split count attn_rmsnorm_matmul chooses when given 0 (negative status on
  * invalid sizes). */
 int attn_rmsnorm_matmul_splits(int B, int H, int D);

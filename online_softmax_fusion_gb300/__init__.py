@@ -65,6 +65,7 @@ SIGNATURES = {
     "attn_rmsnorm_matmul_tiled": (_c_int, [_c_void_p] * 5 + [_c_int] * 3 + [_c_float, _c_int,
                                                                            _c_int, _c_void_p]),
     "attn_rmsnorm_matmul_splits": (_c_int, [_c_int] * 3),
+    "attn_rmsnorm_matmul_chained": (_c_int, [_c_void_p] * 5 + [_c_int] * 3 + [_c_float, _c_void_p]),
     "attn_decode_num_splits": (_c_int, [_c_int] * 5),
     "attn_decode_split_len": (_c_int, [_c_int] * 2),
     "attn_decode_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
@@ -300,7 +301,7 @@ def backward(q, k, v, o, lse, dout, causal=False, scale=None, alibi_slopes=None,
 
 
 def rmsnorm_matmul(x, g, w, eps=0.0, splits=0, out=None, rms=None, with_rms=False,
-                   batch_tile=0):
+                   batch_tile=0, chained=False):
     """Fused RMSNorm + product: O = ((x * g) @ w) / RMS(x), RMS(x) =
     sqrt(mean(x^2) + eps). x [B,H], g [H], w [H,D] bf16 CUDA. Returns
     (O bf16 [B,D], RMS fp32 [B] or None). batch_tile / splits: 0 = auto."""
@@ -315,8 +316,17 @@ def rmsnorm_matmul(x, g, w, eps=0.0, splits=0, out=None, rms=None, with_rms=Fals
         out = torch.empty((B, D), dtype=torch.bfloat16, device=x.device)
     if rms is None and with_rms:
         rms = torch.empty((B,), dtype=torch.float32, device=x.device)
-    st = lib().attn_rmsnorm_matmul_tiled(_ptr(x), _ptr(g), _ptr(w), _ptr(out), _ptr(rms), B, H,
-                                         D, float(eps), int(batch_tile), int(splits), _stream())
+    if chained:
+        # launched as a programmatic dependent of the kernel before it on the
+        # stream; w must not be written by that kernel (automatic tiling)
+        if splits or batch_tile:
+            raise ValueError("chained calls choose their own tiling")
+        st = lib().attn_rmsnorm_matmul_chained(_ptr(x), _ptr(g), _ptr(w), _ptr(out), _ptr(rms),
+                                               B, H, D, float(eps), _stream())
+    else:
+        st = lib().attn_rmsnorm_matmul_tiled(_ptr(x), _ptr(g), _ptr(w), _ptr(out), _ptr(rms), B,
+                                             H, D, float(eps), int(batch_tile), int(splits),
+                                             _stream())
     _check(st, "attn_rmsnorm_matmul")
     return out, rms
 

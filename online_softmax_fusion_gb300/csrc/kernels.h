@@ -118,6 +118,9 @@ struct RmsParams {
     int cvt_warps;                            // converter warps per K step (<= 8)
     int cvt_groups;                           // groups taking K steps in turn; divides x_stages
     int recv_separate;                        // the epilogue's receive area follows the rings
+    int chained;                              // launched as a programmatic dependent of the
+                                              // kernel before it: W streams in at once, X and
+                                              // the outputs wait for that kernel
     float eps;
     int* status;
 };

@@ -183,9 +183,16 @@ __global__ void __launch_bounds__(rm_threads<CVT>(), CVT == 8 ? 2 : 1)
     // the first fill of both rings goes out while TMEM is being allocated:
     // lanes 0.. of warp 0 issue W slots, lanes 16.. issue X slots
     const int w_first = min(NW, nk), x_first = min(NX, nk);
+    if (p.chained && threadIdx.x == 0) {
+        // the next call on the stream may start its own W stream now
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
     if (warp == 0) {
         __syncwarp();
         if (lane < w_first) issue_w(lane);
+        // chained: X (and G) may be written by the kernel before this one on
+        // the stream, which may still run; W is not (the caller's promise)
+        if (p.chained && lane >= 16) asm volatile("griddepcontrol.wait;" ::: "memory");
         if (lane >= 16 && lane - 16 < x_first) issue_x(lane - 16);
     }
     if (warp == 1) {
@@ -212,6 +219,7 @@ __global__ void __launch_bounds__(rm_threads<CVT>(), CVT == 8 ? 2 : 1)
     } else if (warp == 2) {
         // ======================================== TMA producer of X and G
         if (lane == 0) {
+            if (p.chained) asm volatile("griddepcontrol.wait;" ::: "memory");
             for (int i = NX; i < nk; ++i) {
                 const int st = i % NX;
                 if (!mbar_wait(&sm.xempty[st], ((i / NX) - 1) & 1, abort, p.status)) break;
@@ -410,6 +418,9 @@ __global__ void __launch_bounds__(rm_threads<CVT>(), CVT == 8 ? 2 : 1)
     }
     tc::fence_before_sync();
     cluster_sync_all();   // every push of every CTA of the cluster has landed
+    // chained: O and RMS may be read or written by the kernel before this
+    // one on the stream; it has finished once this wait returns
+    if (p.chained) asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- merge the per-row statistics of the cluster (local)
     const int* re = reinterpret_cast<const int*>(recv + e_off);
@@ -522,13 +533,15 @@ int launch_t(const RmsLaunch& L, int dev, cudaStream_t stream) {
     cfg.blockDim = dim3(rm_threads<CVT>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = unsigned(p.splits);
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.chained ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, rmsnorm_matmul_kernel<CVT>, L.tmX, L.tmW, p) != cudaSuccess) {
         (void)cudaGetLastError();
         return ATTN_ERR_CUDA;

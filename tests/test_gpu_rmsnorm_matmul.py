@@ -162,3 +162,48 @@ def test_full_size_sampled_rows(name):
     ref = rmsnorm_matmul_ref(xs, d["g"].cpu(), d["w"].cpu())
     _check(O, ref, rows=rows)
     np.testing.assert_allclose(rms.cpu().numpy()[rows], rms_ref(xs), rtol=2e-5)
+
+
+# --------------------------------------------- chained (programmatic) launches
+@pytest.mark.parametrize("B,H,D", [(16, 4096, 4096), (5, 328, 328), (256, 1024, 1024)])
+def test_chained_stack_of_layers(B, H, D):
+    """Each call's X is the previous call's output (read after write across
+    launches that may overlap): every layer matches the oracle on the exact
+    input it was given, and bit for bit the same call launched plainly."""
+    x, g, _ = _inputs(B, H, D, 7)
+    ws = [_inputs(B, H, D, 20 + i)[2] for i in range(4)]   # square W: O feeds the next X
+    outs, rms = [], []
+    cur = x
+    for w in ws:
+        O, R = attn.rmsnorm_matmul(cur, g, w, with_rms=True, chained=True)
+        outs.append(O)
+        rms.append(R)
+        cur = O
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    cur = x
+    for w, O, R in zip(ws, outs, rms):
+        ref = rmsnorm_matmul_ref(cur, g, w)
+        _check(O, ref)
+        assert np.allclose(R.cpu().numpy(), rms_ref(cur), rtol=2e-5, atol=0)
+        O_plain, R_plain = attn.rmsnorm_matmul(cur, g, w, with_rms=True)
+        torch.cuda.synchronize()
+        assert torch.equal(O, O_plain) and torch.equal(R, R_plain)
+        cur = O
+
+
+def test_chained_overwrites_the_previous_input():
+    """A chained call may start while the call before it still runs; its
+    outputs wait for that call, so writing over the previous call's X
+    (write after read) leaves the previous result intact."""
+    B, H, D = 16, 4096, 4096
+    xa, g, w = _inputs(B, H, D, 31)
+    xb = _inputs(B, H, D, 32)[0]
+    xa_host = xa.cpu()
+    Oa = torch.empty((B, D), dtype=torch.bfloat16, device=DEV)
+    attn.rmsnorm_matmul(xa, g, w, out=Oa, chained=True)
+    attn.rmsnorm_matmul(xb, g, w, out=xa, chained=True)     # writes over xa
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    _check(Oa, rmsnorm_matmul_ref(xa_host, g, w))
+    _check(xa[:, :D], rmsnorm_matmul_ref(xb, g, w))
