@@ -857,9 +857,12 @@ def run_ours(args):
     pc = W.PREFILL_CONFIGS[PREFILL_WORKLOAD]
     dc = W.DECODE_CONFIGS[DECODE_WORKLOAD]
     if args.small:
-        # same distribution, a quarter of the batch: ~2 GB of K/V on the device
+        # same distributions, smaller batches for profiling captures: ~2 GB of
+        # K/V for the decode, one sequence (134 MB of Q/K/V) for the prefill
         dc = W.DecodeConfig(dc.name + "_b16", B=16, Hq=dc.Hq, Hkv=dc.Hkv, Lk_max=dc.Lk_max,
                             d=dc.d, len_lo=dc.len_lo, len_hi=dc.len_hi, seed=dc.seed)
+        pc = W.PrefillConfig(pc.name + "_b1", B=1, Hq=pc.Hq, Hkv=pc.Hkv, Lq=pc.Lq, Lk=pc.Lk,
+                             d=pc.d, causal=pc.causal, seed=pc.seed)
     launches = []
     if do_p:
         pin = W.make_prefill_inputs(pc, dev)
@@ -999,7 +1002,7 @@ def run_ours(args):
             roof = {"bound": "tensor", "achieved": achieved, "peak": pk_t, "unit": "TFLOP/s",
                     "frac": achieved / pk_t,
                     "traffic": recorded_traffic("prefill",
-                                                "online_softmax_fusion_gb300/csrc/prefill_tc.cu"),
+                                                "online_softmax_fusion_gb300/csrc/prefill_tc.cuh"),
                     "peak_kind": f"{peak_src} bf16 burst",
                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                     "kernel": "prefill_tc_kernel", "ms_per_launch": per["prefill"]}
@@ -1054,7 +1057,8 @@ def main(argv=None):
                     help="batch rows of the RMSNorm + MatMul workload (--kernel rmsnorm), batch "
                          "of the causal MHA backward (--kernel backward)")
     ap.add_argument("--small", action="store_true",
-                    help="decode on a quarter of the batch (profiling captures)")
+                    help="decode on a quarter of the batch, prefill on one sequence "
+                         "(profiling captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
