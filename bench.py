@@ -978,9 +978,37 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+        # the host link's own ceiling for the same bytes: the step's copies
+        # alone (no kernels), inputs in on one stream while the outputs go
+        # out on another, as the pipelined entry overlaps them
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+        def copies_only():
+            with torch.cuda.stream(s_in):
+                q.copy_(hq, non_blocking=True)
+                k.copy_(hk, non_blocking=True)
+                v.copy_(hv, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                ho.copy_(O, non_blocking=True)
+                hl.copy_(LSE, non_blocking=True)
+        copies_only()
+        torch.cuda.synchronize()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(e2e_steps):
+            s_in.wait_stream(stream)
+            s_out.wait_stream(stream)
+            copies_only()
+            stream.wait_stream(s_in)
+            stream.wait_stream(s_out)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        link_ms = c0.elapsed_time(c1) / e2e_steps
         e2e = {"value": fl * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": (hq.numel() + hk.numel() + hv.numel()) * 2,
-               "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4, "ms_per_step": e2e_ms}
+               "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4, "ms_per_step": e2e_ms,
+               "copies_only_ms": link_ms, "of_copies_only": link_ms / e2e_ms}
         del hq, hk, hv, ho, hl, ws
 
     others = None
