@@ -516,13 +516,25 @@ def measure_other_workloads(attn, W, dev, peaks, checks):
         wcopies = [rin["w"]] + [rin["w"].clone() for _ in range(4)]
         Orm = torch.empty((cfg.B, cfg.D), dtype=torch.bfloat16, device=dev)
 
+        wsb = torch.empty((attn.rmsnorm_matmul_ws_bytes(cfg.B, cfg.H),), dtype=torch.uint8,
+                          device=dev)
+
         def fn_rms(chained):
             for wc in wcopies:
                 attn.rmsnorm_matmul(rin["x"], rin["g"], wc, out=Orm, chained=chained)
+
+        def fn_ws():
+            for wc in wcopies:
+                attn.rmsnorm_matmul(rin["x"], rin["g"], wc, out=Orm, form="auto", workspace=wsb)
         ms_plain = graph_time(lambda: fn_rms(False), 4, replays=5) / len(wcopies)
         # a stack of calls with constant weights: each launch overlaps the
         # end of the one before (programmatic dependent launch)
-        ms = graph_time(lambda: fn_rms(True), 4, replays=5) / len(wcopies)
+        ms_chained = graph_time(lambda: fn_rms(True), 4, replays=5) / len(wcopies)
+        # the workspace entry (two-pass form for batch tiles of 128 rows and more)
+        ms_ws = graph_time(fn_ws, 4, replays=5) / len(wcopies)
+        two_pass = attn.lib().attn_rmsnorm_matmul_ws_bytes(cfg.B, cfg.H) > 0 and cfg.B >= 128
+        ms = min(ms_chained, ms_ws)
+        form = "chained" if ms_chained <= ms_ws else ("two_pass" if two_pass else "fused")
         byts = rmsnorm_matmul_bytes(cfg.B, cfg.H, cfg.D)
         fl = rmsnorm_matmul_flops(cfg.B, cfg.H, cfg.D)
         gbs = byts / (ms * 1e-3) / 1e9
@@ -531,9 +543,11 @@ def measure_other_workloads(attn, W, dev, peaks, checks):
                     "gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "tflops": tf,
                     "frac_bf16": tf / peaks["bf16_tflops"], "bytes": byts, "flops": fl,
                     "splits": attn.lib().attn_rmsnorm_matmul_splits(cfg.B, cfg.H, cfg.D),
-                    "ms_single_launch": ms_plain,
-                    "timing": "cuda graph replay of back-to-back chained calls, W rotated over "
-                              "5 copies (> L2); ms_single_launch: the same calls launched plainly"})
+                    "ms_single_launch": ms_plain, "ms_chained": ms_chained,
+                    "ms_workspace_entry": ms_ws, "form": form,
+                    "timing": "cuda graph replay of 5 back-to-back calls, W rotated over 5 "
+                              "copies (> L2); ms = the faster of the chained calls and the "
+                              "workspace entry (form names it); ms_single_launch: plain calls"})
         checks.append({"workload": name, "kind": "rmsnorm", "x": rin["x"][:3].cpu(),
                        "g": rin["g"].cpu(), "w": rin["w"].cpu(), "O": Orm[:3].cpu()})
         del rin, wcopies, Orm
@@ -789,8 +803,15 @@ def run_rmsnorm(args):
     stream = torch.cuda.current_stream()
     it = [0]
 
+    wsb = torch.empty((attn.rmsnorm_matmul_ws_bytes(cfg.B, cfg.H),), dtype=torch.uint8,
+                      device="cuda")
+
     def step():
-        attn.rmsnorm_matmul(rin["x"], rin["g"], wcopies[it[0] % 5], out=O)
+        if args.rms_form:
+            attn.rmsnorm_matmul(rin["x"], rin["g"], wcopies[it[0] % 5], out=O,
+                                form=args.rms_form, workspace=wsb)
+        else:
+            attn.rmsnorm_matmul(rin["x"], rin["g"], wcopies[it[0] % 5], out=O)
         it[0] += 1
     ms = time_launches(step, args.steps, args.warmup, stream)
     byts = rmsnorm_matmul_bytes(cfg.B, cfg.H, cfg.D)
@@ -798,6 +819,7 @@ def run_rmsnorm(args):
     gbs = byts / (ms * 1e-3) / 1e9
     print(json.dumps({"metric": "RMSNorm+MatMul GB/s", "value": gbs, "unit": "GB/s",
                       "workload": cfg.name, "ms_per_launch": ms,
+                      "form": args.rms_form or "fused (single kernel)",
                       "frac_hbm": gbs / peaks["hbm_gbs"],
                       "tflops": fl / (ms * 1e-3) / 1e12, "steps": args.steps,
                       "warmup": args.warmup, "timing": "eager launches, CUDA events"}),
@@ -1076,6 +1098,9 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rms-form", choices=["auto", "fused", "two_pass"], default=None,
+                    help="--kernel rmsnorm: call the workspace entry with this form "
+                         "(default: the single fused kernel)")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip the secondary GQA sweep / long-decode measurements")
     ap.add_argument("--kernel", choices=["all", "prefill", "decode", "rmsnorm", "backward"],

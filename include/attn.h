@@ -295,6 +295,37 @@ int attn_rmsnorm_matmul_tiled(const void* X, const void* G, const void* W, void*
 int attn_rmsnorm_matmul_chained(const void* X, const void* G, const void* W, void* O, float* rms,
                                 int B, int H, int D, float eps, void* stream);
 
+/*
+ * attn_rmsnorm_matmul_ws - attn_rmsnorm_matmul with a workspace, which lets
+ * large batches take a two-pass form (no counterpart in the pages: the same
+ * operation, O = ((X ⊙ G) W) / RMS(X), split into two launches).
+ *
+ * Forms:
+ *   ATTN_RMS_FORM_FUSED     the single kernel of attn_rmsnorm_matmul, which
+ *                           converts X ⊙ G and sums squares inside the
+ *                           product loop (workspace unused, may be NULL)
+ *   ATTN_RMS_FORM_TWO_PASS  a conversion pass writes X ⊙ G (bf16) and each
+ *                           row's repaired sum of squares (E, s) to the
+ *                           workspace; the product kernel follows it as a
+ *                           programmatic dependent and runs with no converter
+ *                           stage. Same operands to the tensor core as the
+ *                           fused form (X ⊙ G rounded to bf16 once); RMS may
+ *                           differ from the fused form's in the last bits
+ *                           (another summation order)
+ *   ATTN_RMS_FORM_AUTO      two-pass when the batch tile is 128 rows or more
+ *                           (the fused converters limit large tiles), else fused
+ *   workspace        device, >= attn_rmsnorm_matmul_ws_bytes(B, H) bytes,
+ *                    16-byte aligned, caller-owned; contents are scratch
+ * Other arguments, results and errors as attn_rmsnorm_matmul (automatic
+ * batch tile and K split); ATTN_ERR_WORKSPACE if the workspace is too small,
+ * ATTN_ERR_VALUE for an unknown form.
+ */
+enum { ATTN_RMS_FORM_AUTO = 0, ATTN_RMS_FORM_FUSED = 1, ATTN_RMS_FORM_TWO_PASS = 2 };
+size_t attn_rmsnorm_matmul_ws_bytes(int B, int H);
+int attn_rmsnorm_matmul_ws(const void* X, const void* G, const void* W, void* O, float* rms,
+                           int B, int H, int D, float eps, int form, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
 /* The split count attn_rmsnorm_matmul chooses when given 0 (negative status on
  * invalid sizes). */
 int attn_rmsnorm_matmul_splits(int B, int H, int D);

@@ -66,6 +66,10 @@ SIGNATURES = {
                                                                            _c_int, _c_void_p]),
     "attn_rmsnorm_matmul_splits": (_c_int, [_c_int] * 3),
     "attn_rmsnorm_matmul_chained": (_c_int, [_c_void_p] * 5 + [_c_int] * 3 + [_c_float, _c_void_p]),
+    "attn_rmsnorm_matmul_ws_bytes": (ctypes.c_size_t, [_c_int] * 2),
+    "attn_rmsnorm_matmul_ws": (_c_int, [_c_void_p] * 5 + [_c_int] * 3 + [_c_float, _c_int,
+                                                                       _c_void_p, ctypes.c_size_t,
+                                                                       _c_void_p]),
     "attn_decode_num_splits": (_c_int, [_c_int] * 5),
     "attn_decode_split_len": (_c_int, [_c_int] * 2),
     "attn_decode_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
@@ -300,11 +304,21 @@ def backward(q, k, v, o, lse, dout, causal=False, scale=None, alibi_slopes=None,
     return dq, dk, dv
 
 
+RMS_FORMS = {"auto": 0, "fused": 1, "two_pass": 2}
+
+
+def rmsnorm_matmul_ws_bytes(B, H) -> int:
+    return int(lib().attn_rmsnorm_matmul_ws_bytes(B, H))
+
+
 def rmsnorm_matmul(x, g, w, eps=0.0, splits=0, out=None, rms=None, with_rms=False,
-                   batch_tile=0, chained=False):
+                   batch_tile=0, chained=False, form=None, workspace=None):
     """Fused RMSNorm + product: O = ((x * g) @ w) / RMS(x), RMS(x) =
     sqrt(mean(x^2) + eps). x [B,H], g [H], w [H,D] bf16 CUDA. Returns
-    (O bf16 [B,D], RMS fp32 [B] or None). batch_tile / splits: 0 = auto."""
+    (O bf16 [B,D], RMS fp32 [B] or None). batch_tile / splits: 0 = auto.
+    form: None = the single fused kernel; "auto" / "fused" / "two_pass" go
+    through the workspace entry (a separate conversion pass for large batch
+    tiles); workspace: uint8 CUDA tensor, allocated when not given."""
     _req(x, "x", torch.bfloat16, 2)
     _req(g, "g", torch.bfloat16, 1)
     _req(w, "w", torch.bfloat16, 2)
@@ -316,7 +330,18 @@ def rmsnorm_matmul(x, g, w, eps=0.0, splits=0, out=None, rms=None, with_rms=Fals
         out = torch.empty((B, D), dtype=torch.bfloat16, device=x.device)
     if rms is None and with_rms:
         rms = torch.empty((B,), dtype=torch.float32, device=x.device)
-    if chained:
+    if form is not None:
+        if chained or splits or batch_tile:
+            raise ValueError("the workspace entry chooses its own tiling")
+        if form not in RMS_FORMS:
+            raise ValueError(f"form must be one of {sorted(RMS_FORMS)}")
+        nbytes = rmsnorm_matmul_ws_bytes(B, H)
+        if workspace is None:
+            workspace = torch.empty((max(nbytes, 1),), dtype=torch.uint8, device=x.device)
+        st = lib().attn_rmsnorm_matmul_ws(_ptr(x), _ptr(g), _ptr(w), _ptr(out), _ptr(rms), B, H,
+                                          D, float(eps), RMS_FORMS[form], _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _stream())
+    elif chained:
         # launched as a programmatic dependent of the kernel before it on the
         # stream; w must not be written by that kernel (automatic tiling)
         if splits or batch_tile:

@@ -481,7 +481,11 @@ int attn_rmsnorm_matmul(const void* X, const void* G, const void* W, void* O, fl
 namespace {
 int rmsnorm_matmul_impl(const void* X, const void* G, const void* W, void* O, float* rms,
                         int B, int H, int D, float eps, int batch_tile, int splits, int chained,
-                        void* stream);
+                        void* stream, void* workspace = nullptr);
+
+// workspace of the two-pass form: Xg [B, H] bf16, then E [B] int, then s [B] fp32
+size_t rms_ws_xg_bytes(int B, int H) { return (size_t(B) * size_t(H) * 2u + 255u) & ~size_t(255); }
+size_t rms_ws_vec_bytes(int B) { return (size_t(B) * 4u + 255u) & ~size_t(255); }
 }  // namespace
 
 extern "C" {
@@ -497,13 +501,37 @@ int attn_rmsnorm_matmul_chained(const void* X, const void* G, const void* W, voi
     return rmsnorm_matmul_impl(X, G, W, O, rms, B, H, D, eps, 0, 0, 1, stream);
 }
 
+size_t attn_rmsnorm_matmul_ws_bytes(int B, int H) {
+    if (B <= 0 || H <= 0) return 0;
+    return rms_ws_xg_bytes(B, H) + 2 * rms_ws_vec_bytes(B);
+}
+
+int attn_rmsnorm_matmul_ws(const void* X, const void* G, const void* W, void* O, float* rms,
+                           int B, int H, int D, float eps, int form, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    if (form < ATTN_RMS_FORM_AUTO || form > ATTN_RMS_FORM_TWO_PASS) return ATTN_ERR_VALUE;
+    if (form == ATTN_RMS_FORM_AUTO) {
+        if (B <= 0 || H <= 0 || D <= 0) return ATTN_ERR_SHAPE;
+        // the fused converters keep up with the tensor core for batch tiles
+        // below 128 rows; from there the separate conversion pass is faster
+        form = rms_geometry(B, H, D, 0, 0).NB >= 128 ? ATTN_RMS_FORM_TWO_PASS
+                                                    : ATTN_RMS_FORM_FUSED;
+    }
+    if (form == ATTN_RMS_FORM_FUSED)
+        return rmsnorm_matmul_impl(X, G, W, O, rms, B, H, D, eps, 0, 0, 0, stream);
+    if (!workspace) return ATTN_ERR_NULL;
+    if (B > 0 && H > 0 && workspace_bytes < attn_rmsnorm_matmul_ws_bytes(B, H))
+        return ATTN_ERR_WORKSPACE;
+    return rmsnorm_matmul_impl(X, G, W, O, rms, B, H, D, eps, 0, 0, 0, stream, workspace);
+}
+
 }  // extern "C"
 
 namespace {
 
 int rmsnorm_matmul_impl(const void* X, const void* G, const void* W, void* O, float* rms,
                         int B, int H, int D, float eps, int batch_tile, int splits, int chained,
-                        void* stream) {
+                        void* stream, void* workspace) {
     if (!X || !G || !W || !O) return ATTN_ERR_NULL;
     if (B <= 0 || H <= 0 || D <= 0) return ATTN_ERR_SHAPE;
     if (B > 65535 * 256 || H > (1 << 30) || D > (1 << 30)) return ATTN_ERR_SHAPE;
@@ -517,6 +545,7 @@ int rmsnorm_matmul_impl(const void* X, const void* G, const void* W, void* O, fl
     for (const void* p : ptrs)
         if (!aligned16(p)) return ATTN_ERR_ALIGN;
     if (rms && (reinterpret_cast<uintptr_t>(rms) & 3u)) return ATTN_ERR_ALIGN;
+    if (workspace && !aligned16(workspace)) return ATTN_ERR_ALIGN;
     // chained calls take the same geometry as plain ones (same result, bit
     // for bit); a grid of one CTA per SM, leaving the second slot to the next
     // call, measured slower (13.1 against 10.7 us at batch 16)
@@ -542,9 +571,29 @@ int rmsnorm_matmul_impl(const void* X, const void* G, const void* W, void* O, fl
     L.p.eps = eps;
     L.p.status = status_ptr();
     int st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (workspace) {
+        // two-pass form: the conversion pass writes X ⊙ G and the per-row
+        // (E, s); the product kernel follows it as a programmatic dependent
+        // (W streams in while the pass runs) and reads the converted X
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        auto* xg = reinterpret_cast<__nv_bfloat16*>(ws);
+        auto* e = reinterpret_cast<int*>(ws + rms_ws_xg_bytes(B, H));
+        auto* sq = reinterpret_cast<float*>(ws + rms_ws_xg_bytes(B, H) + rms_ws_vec_bytes(B));
+        if ((st = make_map(&L.tmX, xg, H, B, 1, g.NB))) return st;
+        if ((st = make_map(&L.tmW, W, D, H, 1, 64))) return st;
+        if ((st = launch_rmsnorm_prep(static_cast<const __nv_bfloat16*>(X),
+                                      static_cast<const __nv_bfloat16*>(G), xg, e, sq, B, H, cs)))
+            return st;
+        L.p.pre = 1;
+        L.p.stats_e = e;
+        L.p.stats_s = sq;
+        L.p.chained = 1;
+        return launch_rmsnorm_matmul(L, cs);
+    }
     if ((st = make_map(&L.tmX, X, H, B, 1, g.NB))) return st;
     if ((st = make_map(&L.tmW, W, D, H, 1, 64))) return st;
-    return launch_rmsnorm_matmul(L, static_cast<cudaStream_t>(stream));
+    return launch_rmsnorm_matmul(L, cs);
 }
 
 }  // namespace

@@ -118,6 +118,9 @@ struct RmsParams {
     int cvt_warps;                            // converter warps per K step (<= 8)
     int cvt_groups;                           // groups taking K steps in turn; divides x_stages
     int recv_separate;                        // the epilogue's receive area follows the rings
+    int pre;                                  // X arrives as X ⊙ G (workspace) with each row's
+    const int* stats_e;                       //   reference exponent E and sum s of (x 2^-E)^2
+    const float* stats_s;                     //   from the conversion pass: no converter work
     int chained;                              // launched as a programmatic dependent of the
                                               // kernel before it: W streams in at once, X and
                                               // the outputs wait for that kernel
@@ -133,5 +136,8 @@ struct RmsLaunch {
 constexpr int kRmsMaxWStages = 12;
 constexpr int kRmsMaxXStages = 8;
 int launch_rmsnorm_matmul(const RmsLaunch& L, cudaStream_t stream);
+// The conversion pass: Xg = X ⊙ G (bf16) and per row (E, s), one warp per row.
+int launch_rmsnorm_prep(const __nv_bfloat16* X, const __nv_bfloat16* G, __nv_bfloat16* Xg,
+                        int* e_out, float* s_out, int B, int H, cudaStream_t stream);
 
 }  // namespace attn

@@ -40,6 +40,12 @@
 // shared memory (distributed shared memory stores); after one cluster
 // barrier each CTA sums its slice of output features from its own shared
 // memory, scales it and stores bf16.
+//
+// Two-pass form (large batch tiles): a conversion pass writes X ⊙ G and
+// the whole rows' (E, s) to a workspace; the product kernel then loads the
+// converted X straight into the MMA operand ring, its converter warps only
+// turn the row statistics into scales while the product runs, and the
+// epilogue exchanges partial tiles alone.
 #include <algorithm>
 
 #include "common.cuh"
@@ -109,6 +115,40 @@ __device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
     return d;
 }
 
+// 2^k for k <= 127 (exact), 0 below the normal range: the repair's factor
+// 2^(2 (E_part - E_max)) only shrinks, and a part that small next to the
+// largest one (whose scaled sum is >= 1/4) is below fp32 resolution anyway.
+__device__ __forceinline__ float pow2i(int k) {
+    return k < -126 ? 0.f : __int_as_float((127 + min(k, 127)) << 23);
+}
+
+// The scalar tail for references far from 1 (|E| > 40), in fp64; kept out
+// of line so that the common path's code stays short.
+__device__ __noinline__ void row_scale_wide(int em, float t, float eps, float* cf, float* rms) {
+    const double td = double(t);
+    *cf = float(1.0 / sqrt(td + ldexp(double(eps), -2 * em)));
+    *rms = float(sqrt(ldexp(td, 2 * em) + double(eps)));
+}
+
+// The scalar tail of one row from its merged (E, s): O = acc * pf * cf with
+// pf = 2^-E and cf = 1 / sqrt(s / H + eps 2^-2E); rms = sqrt(s 2^2E / H + eps).
+__device__ __forceinline__ void row_scale(int em, float ss, int H, float eps, float& pf, float& cf,
+                                          float& rms) {
+    pf = 0.f;
+    cf = 0.f;
+    rms = sqrtf(eps);
+    if (ss > 0.f) {
+        const float t = ss / float(H);
+        pf = ldexpf(1.f, -em);      // subnormal for E > 126 (inputs near the bf16 maximum)
+        if (em >= -40 && em <= 40) {
+            cf = rsqrtf(t + eps * pow2i(-2 * em));
+            rms = sqrtf(t * pow2i(2 * em) + eps);
+        } else {
+            row_scale_wide(em, t, eps, &cf, &rms);
+        }
+    }
+}
+
 // sum of (x * sc)^2 over the two bf16 values of a word
 __device__ __forceinline__ float sq2(uint32_t w, float sc, float acc) {
     const float lo = __uint_as_float(w << 16) * sc;
@@ -142,8 +182,9 @@ __global__ void __launch_bounds__(rm_threads<CVT>(), CVT == 8 ? 2 : 1)
     const int b0 = blockIdx.y * NB;
     const uint32_t rank = cluster_rank();
     const int S = p.splits;
-    const int kt0 = int((long long)rank * p.k_tiles / S);
-    const int kt1 = int((long long)(rank + 1) * p.k_tiles / S);
+    // k_tiles * S < 2^31 (the host bounds H): 32-bit division
+    const int kt0 = int(rank) * p.k_tiles / S;
+    const int kt1 = (int(rank) + 1) * p.k_tiles / S;
     const int nk = kt1 - kt0;
     uint32_t ncols = 32;
     while (ncols < uint32_t(NB)) ncols <<= 1;
@@ -159,9 +200,15 @@ __global__ void __launch_bounds__(rm_threads<CVT>(), CVT == 8 ? 2 : 1)
     auto issue_x = [&](int i) {
         const int s = i % NX;
         const int k = (kt0 + i) * 64;
-        const uint32_t gbytes = uint32_t(min(64, p.H - k)) * 2u;
-        mbar_arrive_expect_tx(&sm.xfull[s], xbytes + gbytes);
-        bulk_load(sm.gbuf[s], p.G + k, gbytes, &sm.xfull[s]);
+        if (p.pre) {
+            // X ⊙ G was formed by the conversion pass: the tile goes straight
+            // to the product
+            mbar_arrive_expect_tx(&sm.xfull[s], xbytes);
+        } else {
+            const uint32_t gbytes = uint32_t(min(64, p.H - k)) * 2u;
+            mbar_arrive_expect_tx(&sm.xfull[s], xbytes + gbytes);
+            bulk_load(sm.gbuf[s], p.G + k, gbytes, &sm.xfull[s]);
+        }
         tma_load_3d(xring + size_t(s) * xbytes, &tmX, &sm.xfull[s], k, b0, 0);
     };
     if (threadIdx.x == 0) {
@@ -234,7 +281,9 @@ __global__ void __launch_bounds__(rm_threads<CVT>(), CVT == 8 ? 2 : 1)
         const uint64_t b0d = tc::sdesc_sw128(smem_u32(xring), 16, 1024);
         for (int i = 0; i < nk; ++i) {
             const int sw = i % NW, sx = i % NX;
-            if (!mbar_wait_warp(&sm.xready[sx], (i / NX) & 1, abort, p.status)) break;
+            if (!mbar_wait_warp(p.pre ? &sm.xfull[sx] : &sm.xready[sx], (i / NX) & 1, abort,
+                                p.status))
+                break;
             if (!mbar_wait_warp(&sm.wfull[sw], (i / NW) & 1, abort, p.status)) break;
             tc::fence_after_sync();
             const uint64_t wo = uint64_t((uint32_t(sw) * kWStageBytes) >> 4);
@@ -264,7 +313,20 @@ __global__ void __launch_bounds__(rm_threads<CVT>(), CVT == 8 ? 2 : 1)
         const int ngroups = p.cvt_groups;
         const int grp = cw / gw;
         const int r = (cw % gw) * 32 + lane;            // batch row of the tile
-        if (grp < ngroups) {
+        if (p.pre) {
+            // the conversion pass gives (E, s) of whole rows: the row scales
+            // are final while the product still runs, and nothing is merged
+            if (p.chained) asm volatile("griddepcontrol.wait;" ::: "memory");
+            for (int rr = cw * 32 + lane; rr < NB; rr += CVT * 32) {
+                const bool in = b0 + rr < p.B;
+                float pf, cf, rms;
+                row_scale(in ? p.stats_e[b0 + rr] : kEmptyExp, in ? p.stats_s[b0 + rr] : 0.f,
+                          p.H, p.eps, pf, cf, rms);
+                sm.row_p[rr] = pf;
+                sm.row_c[rr] = cf;
+                if (p.rms && blockIdx.x == 0 && rank == 0 && in) p.rms[b0 + rr] = rms;
+            }
+        } else if (grp < ngroups) {
             int E = kEmptyExp;      // reference exponent: |x| < 2^E for every x seen
             float Ssum = 0.f;       // sum of (x 2^-E)^2
             float SC2 = 0.f;        // 2^-2E, set whenever E changes
@@ -359,12 +421,12 @@ __global__ void __launch_bounds__(rm_threads<CVT>(), CVT == 8 ? 2 : 1)
         }
         converter_sync<CVT>();
         // merge the groups (the split form of the repair, inside the CTA)
-        for (int r = cw * 32 + lane; r < NB; r += CVT * 32) {
+        for (int r = cw * 32 + lane; r < NB && !p.pre; r += CVT * 32) {
             int em = kEmptyExp;
             for (int q = 0; q < ngroups; ++q) em = max(em, sm.part_e[q * NB + r]);
             float ss = 0.f;
             for (int q = 0; q < ngroups; ++q)
-                ss += ldexpf(sm.part_s[q * NB + r], 2 * (sm.part_e[q * NB + r] - em));
+                ss += sm.part_s[q * NB + r] * pow2i(2 * (sm.part_e[q * NB + r] - em));
             sm.row_e[r] = em;
             sm.row_s[r] = ss;
         }
@@ -409,7 +471,7 @@ __global__ void __launch_bounds__(rm_threads<CVT>(), CVT == 8 ? 2 : 1)
                 st_cluster_u32(dst + uint32_t((c0 + cc + j) * wd * 4), v[j]);
         }
     }
-    for (int idx = threadIdx.x; idx < S * NB; idx += rm_threads<CVT>()) {
+    for (int idx = threadIdx.x; idx < S * NB && !p.pre; idx += rm_threads<CVT>()) {
         const int q = idx / NB, r = idx - (idx / NB) * NB;
         const uint32_t o = uint32_t((int(rank) * NB + r) * 4);
         const uint32_t base = map_rank(recv_a, uint32_t(q));
@@ -425,26 +487,13 @@ __global__ void __launch_bounds__(rm_threads<CVT>(), CVT == 8 ? 2 : 1)
     // ---- merge the per-row statistics of the cluster (local)
     const int* re = reinterpret_cast<const int*>(recv + e_off);
     const float* rs = reinterpret_cast<const float*>(recv + s_off);
-    for (int r = threadIdx.x; r < NB; r += rm_threads<CVT>()) {
+    for (int r = threadIdx.x; r < NB && !p.pre; r += rm_threads<CVT>()) {
         int em = kEmptyExp;
         for (int q = 0; q < S; ++q) em = max(em, re[q * NB + r]);
         float ss = 0.f;
-        for (int q = 0; q < S; ++q) ss += ldexpf(rs[q * NB + r], 2 * (re[q * NB + r] - em));   // the repair
-        // O = (acc 2^-E) / sqrt(s / H + eps 2^-2E); fp32 unless E is extreme
-        float pf = 0.f, cf = 0.f;
-        float rms = sqrtf(p.eps);
-        if (ss > 0.f) {
-            const float t = ss / float(p.H);
-            pf = ldexpf(1.f, -em);
-            if (em >= -40 && em <= 40) {
-                cf = rsqrtf(t + ldexpf(p.eps, -2 * em));
-                rms = sqrtf(ldexpf(t, 2 * em) + p.eps);
-            } else {
-                const double td = double(t);
-                cf = float(1.0 / sqrt(td + ldexp(double(p.eps), -2 * em)));
-                rms = float(sqrt(ldexp(td, 2 * em) + double(p.eps)));
-            }
-        }
+        for (int q = 0; q < S; ++q) ss += rs[q * NB + r] * pow2i(2 * (re[q * NB + r] - em));   // the repair
+        float pf, cf, rms;
+        row_scale(em, ss, p.H, p.eps, pf, cf, rms);
         sm.row_p[r] = pf;
         sm.row_c[r] = cf;
         if (p.rms && blockIdx.x == 0 && rank == 0 && b0 + r < p.B) p.rms[b0 + r] = rms;
@@ -497,6 +546,63 @@ __global__ void __launch_bounds__(rm_threads<CVT>(), CVT == 8 ? 2 : 1)
         tc::fence_after_sync();
         tc::tmem_dealloc(tacc, ncols);
     }
+}
+
+// The conversion pass of the two-kernel form: X ⊙ G rounded to bf16 (the
+// product's operand, the same rounding as the fused converter) and, per row,
+// the reference exponent E (2^E above the row's largest |x|) and the sum s of
+// (x 2^-E)^2 (exact power-of-two scaling: no square can overflow). One warp
+// per row; the row is read twice (the second time from L1/L2).
+__global__ void __launch_bounds__(256) rms_prep_kernel(const __nv_bfloat16* __restrict__ X,
+                                                       const __nv_bfloat16* __restrict__ G,
+                                                       __nv_bfloat16* __restrict__ Xg,
+                                                       int* __restrict__ e_out,
+                                                       float* __restrict__ s_out, int B, int H) {
+    // the product kernel, launched as this kernel's dependent, may start
+    // streaming W now; it waits for this grid before reading Xg or (E, s)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int row = int(blockIdx.x) * 8 + int(threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= B) return;
+    const uint4* x = reinterpret_cast<const uint4*>(X + size_t(row) * H);
+    const uint4* g = reinterpret_cast<const uint4*>(G);
+    uint4* xg = reinterpret_cast<uint4*>(Xg + size_t(row) * H);
+    const int nc = H / 8;
+    uint32_t mm = 0u;
+    for (int c = lane; c < nc; c += 32) {
+        const uint4 v = x[c];
+        mm = bf16x2_maxabs(mm, bf16x2_maxabs(bf16x2_maxabs(v.x, v.y), bf16x2_maxabs(v.z, v.w)));
+    }
+    mm &= 0x7fff7fffu;
+    uint32_t mb = max(mm & 0xffffu, mm >> 16);
+    for (int o = 16; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    const int E = mb != 0u ? max(int(mb >> 7) - 126, kMinExp) : kEmptyExp;
+    const float sc = mb != 0u ? ldexpf(1.f, -E) : 0.f;
+    float acc = 0.f;
+    for (int c = lane; c < nc; c += 32) {
+        uint4 v = x[c];
+        acc = sq2(v.x, sc, acc);
+        acc = sq2(v.y, sc, acc);
+        acc = sq2(v.z, sc, acc);
+        acc = sq2(v.w, sc, acc);
+        const uint4 gg = g[c];
+        v.x = bf16x2_mul(v.x, gg.x);
+        v.y = bf16x2_mul(v.y, gg.y);
+        v.z = bf16x2_mul(v.z, gg.z);
+        v.w = bf16x2_mul(v.w, gg.w);
+        xg[c] = v;
+    }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+        e_out[row] = E;
+        s_out[row] = acc;
+    }
+}
+
+int launch_rmsnorm_prep(const __nv_bfloat16* X, const __nv_bfloat16* G, __nv_bfloat16* Xg,
+                        int* e_out, float* s_out, int B, int H, cudaStream_t stream) {
+    rms_prep_kernel<<<unsigned((B + 7) / 8), 256, 0, stream>>>(X, G, Xg, e_out, s_out, B, H);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 namespace {

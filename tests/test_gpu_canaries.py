@@ -36,13 +36,15 @@ def attn():
 class Guarded:
     """An output tensor with sentinel-filled bands on both sides."""
 
-    def __init__(self, shape, dtype):
+    def __init__(self, shape, dtype, scratch=False):
         self.n = int(math.prod(shape))
         self.buf = torch.empty(self.n + 2 * GUARD, dtype=dtype, device="cuda")
         self.size = self.buf.element_size()
         self._bits().fill_(SENTINEL[self.size])
         self.t = self.buf[GUARD:GUARD + self.n].view(shape)
-        self.t.fill_(float("nan"))
+        self.scratch = scratch      # a workspace: only the bands are checked
+        if not scratch:
+            self.t.fill_(float("nan"))
 
     def _bits(self):
         return self.buf.view(torch.int16 if self.size == 2 else torch.int32)
@@ -54,6 +56,8 @@ class Guarded:
         lo = int((bits[:GUARD] != s).sum())
         hi = int((bits[GUARD + self.n:] != s).sum())
         assert lo == 0 and hi == 0, f"{what}: {lo} elements before and {hi} after it overwritten"
+        if self.scratch:
+            return
         nan = int(torch.isnan(self.t.float()).sum())
         assert nan == 0, f"{what}: {nan} elements never written (NaN left)"
 
@@ -192,15 +196,24 @@ def test_backward_writes_exactly_its_outputs(attn, impl, d, B, Hq, Hkv, Lq, Lk):
     assert attn.device_status() == 0
 
 
-@pytest.mark.parametrize("B,H,D", [(5, 328, 200), (17, 136, 72), (3, 64, 64)])
-def test_rmsnorm_matmul_writes_exactly_its_outputs(attn, B, H, D):
+@pytest.mark.parametrize("form", [None, "two_pass"])
+@pytest.mark.parametrize("B,H,D", [(5, 328, 200), (17, 136, 72), (3, 64, 64), (131, 200, 136)])
+def test_rmsnorm_matmul_writes_exactly_its_outputs(attn, B, H, D, form):
     g = torch.Generator().manual_seed(B * 1000 + H)
     x = torch.randn(B, H, generator=g).to(torch.bfloat16)
     gw = (1 + 0.1 * torch.randn(H, generator=g)).to(torch.bfloat16)
     w = (torch.randn(H, D, generator=g) / H ** 0.5).to(torch.bfloat16)
     O = Guarded((B, D), torch.bfloat16)
     R = Guarded((B,), torch.float32)
-    attn.rmsnorm_matmul(x.cuda(), gw.cuda(), w.cuda(), out=O.t, rms=R.t)
+    if form is None:
+        attn.rmsnorm_matmul(x.cuda(), gw.cuda(), w.cuda(), out=O.t, rms=R.t)
+    else:
+        # the workspace is an output of the conversion pass: guarded too
+        nbytes = attn.rmsnorm_matmul_ws_bytes(B, H)
+        ws = Guarded((nbytes // 4,), torch.int32, scratch=True)
+        attn.rmsnorm_matmul(x.cuda(), gw.cuda(), w.cuda(), out=O.t, rms=R.t, form=form,
+                            workspace=ws.t)
+        ws.check("workspace")
     O.check("O")
     R.check("RMS")
     assert attn.device_status() == 0

@@ -207,3 +207,94 @@ def test_chained_overwrites_the_previous_input():
     assert attn.device_status() == 0
     _check(Oa, rmsnorm_matmul_ref(xa_host, g, w))
     _check(xa[:, :D], rmsnorm_matmul_ref(xb, g, w))
+
+
+# ------------------------------------------- two-pass form (workspace entry)
+TWO_PASS_CASES = [
+    # B, H, D, eps
+    (5, 328, 200, 0.0),           # ragged everywhere
+    (1, 64, 8, 0.0),
+    (16, 512, 256, 1e-5),
+    (128, 768, 136, 0.0),
+    (256, 512, 256, 0.0),
+    (300, 256, 128, 0.5),         # two batch tiles
+    (256, 4096, 1024, 1e-6),      # the K split of a large hidden size
+]
+
+
+@pytest.mark.parametrize("B,H,D,eps", TWO_PASS_CASES)
+def test_two_pass_parity(B, H, D, eps):
+    """The conversion pass + product kernel against the oracle; O agrees with
+    the fused kernel to one bf16 rounding (same tensor-core operands, the
+    per-row scale summed in another order)."""
+    x, g, w = _inputs(B, H, D, seed=B * 31 + H + D)
+    O, rms = attn.rmsnorm_matmul(x, g, w, eps=eps, with_rms=True, form="two_pass")
+    O1, rms1 = attn.rmsnorm_matmul(x, g, w, eps=eps, with_rms=True)
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    ref = rmsnorm_matmul_ref(x.cpu(), g.cpu(), w.cpu(), eps)
+    _check(O, ref)
+    np.testing.assert_allclose(rms.cpu().numpy(), rms_ref(x.cpu(), eps), rtol=2e-5)
+    np.testing.assert_allclose(rms.cpu().numpy(), rms1.cpu().numpy(), rtol=2e-6)
+    diff = torch.abs(O.float() - O1.float())
+    assert torch.all(diff <= 2.0 ** -7 * torch.abs(O1.float()) + 1e-30)
+
+
+def test_two_pass_extreme_magnitudes_and_zero_rows():
+    """Rows at 2^100 (every fp32 square overflows), at 2^-60, all-zero rows,
+    with and without eps, through the conversion pass."""
+    x, g, w = _inputs(140, 1024, 256, seed=41)
+    xf = x.float()
+    xf[0:8] *= 2.0 ** 100
+    xf[8:16] *= 2.0 ** -60
+    xf[16:24, 700:] *= 2.0 ** 20
+    xf[30] = 0
+    xf[139] = 0
+    x2 = xf.to(torch.bfloat16)
+    for eps in (0.0, 1e-4):
+        O, rms = attn.rmsnorm_matmul(x2, g, w, eps=eps, with_rms=True, form="two_pass")
+        torch.cuda.synchronize()
+        assert attn.device_status() == 0
+        assert torch.all(O[30] == 0) and torch.all(O[139] == 0)
+        assert rms[30].item() == pytest.approx(math.sqrt(eps), rel=1e-6, abs=0)
+        xs = x2.cpu()
+        ref = rmsnorm_matmul_ref(xs, g.cpu(), w.cpu(), eps)
+        for rows in (slice(8, 16), slice(16, 140)):
+            _check(O[rows], ref[rows])
+        # the 2^100 rows: O is that of the unscaled rows, RMS scales exactly
+        ref_big = rmsnorm_matmul_ref(x.cpu()[0:8], g.cpu(), w.cpu())
+        _check(O[0:8], ref_big)
+        np.testing.assert_allclose(rms.cpu().numpy()[0:8].astype(np.float64) / 2.0 ** 100,
+                                   rms_ref(x.cpu()[0:8]), rtol=2e-5)
+        keep = [i for i in range(140) if i >= 8]
+        np.testing.assert_allclose(rms.cpu().numpy()[keep], rms_ref(xs, eps)[keep], rtol=2e-5)
+
+
+def test_two_pass_full_size_sampled_rows():
+    """Batch 256 of the LLaMA-2-7B shape through the automatic form (which
+    takes the two-pass path there), the launch the bench times."""
+    cfg = W.RMS_MATMUL_CONFIGS["rmsnorm_matmul_llama7b_b256"]
+    d = W.make_rmsnorm_matmul_inputs(cfg, DEV)
+    O, rms = attn.rmsnorm_matmul(d["x"], d["g"], d["w"], with_rms=True, form="auto")
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    rows = sorted(set([0, 1, cfg.B - 1] + list(
+        np.random.default_rng(12).choice(cfg.B, size=min(cfg.B, 13), replace=False))))
+    xs = d["x"].cpu()[rows]
+    _check(O, rmsnorm_matmul_ref(xs, d["g"].cpu(), d["w"].cpu()), rows=rows)
+    np.testing.assert_allclose(rms.cpu().numpy()[rows], rms_ref(xs), rtol=2e-5)
+
+
+def test_two_pass_rejects_small_workspace_and_unknown_form():
+    x, g, w = _inputs(130, 256, 128, seed=3)
+    nbytes = attn.rmsnorm_matmul_ws_bytes(130, 256)
+    assert nbytes >= 130 * 256 * 2 + 2 * 130 * 4
+    small = torch.empty((nbytes - 16,), dtype=torch.uint8, device=DEV)
+    with pytest.raises(attn.AttnError):
+        attn.rmsnorm_matmul(x, g, w, form="two_pass", workspace=small)
+    with pytest.raises(ValueError):
+        attn.rmsnorm_matmul(x, g, w, form="three_pass")
+    # the fused form through the same entry needs no workspace
+    O, _ = attn.rmsnorm_matmul(x, g, w, form="fused", workspace=small)
+    torch.cuda.synchronize()
+    _check(O, rmsnorm_matmul_ref(x.cpu(), g.cpu(), w.cpu()))
