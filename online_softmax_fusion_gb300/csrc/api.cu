@@ -286,6 +286,7 @@ int prefill_impl(const void* Q, const void* K, const void* V, void* O, float* LS
         if ((st = make_map(&L.tmQ, Q, d, Lq, (long long)B * Hq, kTcBM))) return st;
         if ((st = make_map(&L.tmK, K, d, Lk, (long long)B * Hkv, kTcBN))) return st;
         if ((st = make_map(&L.tmV, V, d, Lk, (long long)B * Hkv, kTcBN))) return st;
+        if ((st = make_map(&L.tmO, O, d, Lq, (long long)B * Hq, 32))) return st;
         const bool one_tile = impl == ATTN_IMPL_TCGEN05_1TILE ||
                               (impl == ATTN_IMPL_AUTO && prefer_one_tile(L.p, d));
         st = one_tile ? launch_prefill_tc1(L, d, s) : launch_prefill_tc(L, d, s);
@@ -353,6 +354,7 @@ int attn_prefill_splitkv(const void* Q, const void* K, const void* V, void* O, f
     if ((st = make_map(&L.tmQ, Q, d, Lq, (long long)B * Hq, kTcBM))) return st;
     if ((st = make_map(&L.tmK, K, d, Lk, (long long)B * Hkv, kTcBN))) return st;
     if ((st = make_map(&L.tmV, V, d, Lk, (long long)B * Hkv, kTcBN))) return st;
+    L.tmO = L.tmQ;   // not read: split partials are written in fp32 without it
     if ((st = launch_prefill_tc(L, d, s))) return st;
     // the partials of each row merged with the split-K combine (rows act as heads)
     if ((long long)B * Hq > 0x7fffffffLL / Lq) return ATTN_ERR_SHAPE;

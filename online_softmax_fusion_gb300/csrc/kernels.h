@@ -56,6 +56,7 @@ struct PrefillLaunch {
     CUtensorMap tmQ;          // Q as (d, Lq, B*Hq), box (64, BM, 1), 128 B swizzle
     CUtensorMap tmK;          // K as (d, Lk, B*Hkv), box (64, BN, 1)
     CUtensorMap tmV;
+    CUtensorMap tmO;          // O as (d, Lq, B*Hq), box (64, 32, 1): one softmax warp's rows
     PrefillParams p;
 };
 

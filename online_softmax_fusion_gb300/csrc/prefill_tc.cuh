@@ -124,7 +124,8 @@ template <int D, bool CAUSAL, bool ALIBI, int MODE, int NT>
 __global__ void __launch_bounds__(tc_threads<NT>(), NT == 2 ? 1 : 2)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, PrefillParams p) {
+                      const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmO, PrefillParams p) {
     constexpr bool EXTRA = MODE != 0;
     constexpr bool CAPPED = MODE == 2;
     using Cfg = TcCfg<D, NT>;
@@ -557,11 +558,26 @@ __global__ void __launch_bounds__(tc_threads<NT>(), NT == 2 ? 1 : 2)
             ok = mbar_wait_warp_limit(&sm.o_done[t], 0, abort, p.status, wlim);
             tc::fence_after_sync();
         }
+        bool stored = false;   // this lane committed a bulk store
         if (ok && !*abort) {
             const bool valid = row < p.Lq;
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16* orow =
-                p.O + ((size_t(b) * p.Hq + head) * p.Lq + (valid ? row : 0)) * D;
+            // O_t goes out through this tile's Q buffer, free now (the commit
+            // behind o_done covers every product that read Q_t): each warp
+            // writes its 32 rows in the tensor map's 128-byte swizzled layout
+            // and stores them with one bulk tensor copy per 64-column box;
+            // rows past Lq fall outside the map and are not written. Used
+            // where it measured faster: two-tile CTAs whose tiles are two
+            // heads of one row block (they finish together), and the capped
+            // forms; the staggered tiles of unpaired causal CTAs and the
+            // one-tile form store rows straight to global memory (graph
+            // replay, us: paired GQA + ALiBi 2k 40.0 against 41.7 and 4k
+            // 125.9 against 129.1; one-tile cap 30 860 against 899; causal
+            // MHA 4k 413 against 405 and one-tile GQA 1k 20.8 against 20.1
+            // when staged, and 415 against 405 even unused: the staged code
+            // is compiled into the capped and ALiBi variants only)
+            constexpr bool kStageO = CAPPED || ALIBI;
+            const bool staged = kStageO && p.splits <= 1 && (CAPPED || (NT == 2 && pair_heads));
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t rr[32];
@@ -571,19 +587,24 @@ __global__ void __launch_bounds__(tc_threads<NT>(), NT == 2 ? 1 : 2)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) rr[i] = 0u;
                 }
-                if (valid && p.splits > 1) {
-                    // split-KV partial: O / l in fp32, [B, Hq, Lq, splits, D]
-                    float* prow = p.O_part +
-                                  ((((size_t(b) * p.Hq + head) * p.Lq + row) * p.splits) +
-                                   blockIdx.z) * D + c * 32;
+                if (staged) {
+                    uint8_t* srow = sm.q[t][c >> 1] + r * 128;
 #pragma unroll
-                    for (int v4 = 0; v4 < 8; ++v4)
-                        *reinterpret_cast<float4*>(prow + v4 * 4) =
-                            make_float4(__uint_as_float(rr[v4 * 4 + 0]) * inv,
-                                        __uint_as_float(rr[v4 * 4 + 1]) * inv,
-                                        __uint_as_float(rr[v4 * 4 + 2]) * inv,
-                                        __uint_as_float(rr[v4 * 4 + 3]) * inv);
-                } else if (valid) {
+                    for (int v8 = 0; v8 < 4; ++v8) {
+                        uint4 w;
+                        w.x = pack_bf16(__uint_as_float(rr[v8 * 8 + 0]) * inv,
+                                        __uint_as_float(rr[v8 * 8 + 1]) * inv);
+                        w.y = pack_bf16(__uint_as_float(rr[v8 * 8 + 2]) * inv,
+                                        __uint_as_float(rr[v8 * 8 + 3]) * inv);
+                        w.z = pack_bf16(__uint_as_float(rr[v8 * 8 + 4]) * inv,
+                                        __uint_as_float(rr[v8 * 8 + 5]) * inv);
+                        w.w = pack_bf16(__uint_as_float(rr[v8 * 8 + 6]) * inv,
+                                        __uint_as_float(rr[v8 * 8 + 7]) * inv);
+                        const int chunk = (c & 1) * 4 + v8;   // 16-byte chunk of the 128-byte row
+                        *reinterpret_cast<uint4*>(srow + ((chunk ^ (r & 7)) << 4)) = w;
+                    }
+                } else if (valid && p.splits <= 1) {
+                    __nv_bfloat16* orow = p.O + ((size_t(b) * p.Hq + head) * p.Lq + row) * D;
 #pragma unroll
                     for (int v8 = 0; v8 < 4; ++v8) {
                         uint4 w;
@@ -597,6 +618,30 @@ __global__ void __launch_bounds__(tc_threads<NT>(), NT == 2 ? 1 : 2)
                                         __uint_as_float(rr[v8 * 8 + 7]) * inv);
                         *reinterpret_cast<uint4*>(orow + c * 32 + v8 * 8) = w;
                     }
+                } else if (valid) {
+                    // split-KV partial: O / l in fp32, [B, Hq, Lq, splits, D]
+                    float* prow = p.O_part +
+                                  ((((size_t(b) * p.Hq + head) * p.Lq + row) * p.splits) +
+                                   blockIdx.z) * D + c * 32;
+#pragma unroll
+                    for (int v4 = 0; v4 < 8; ++v4)
+                        *reinterpret_cast<float4*>(prow + v4 * 4) =
+                            make_float4(__uint_as_float(rr[v4 * 4 + 0]) * inv,
+                                        __uint_as_float(rr[v4 * 4 + 1]) * inv,
+                                        __uint_as_float(rr[v4 * 4 + 2]) * inv,
+                                        __uint_as_float(rr[v4 * 4 + 3]) * inv);
+                }
+            }
+            if (staged) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+#pragma unroll
+                    for (int bx = 0; bx < D / 64; ++bx)
+                        tma_store_3d(&tmO, sm.q[t][bx] + q4 * 32 * 128, bx * 64,
+                                     row0 + q4 * 32, b * p.Hq + head);
+                    bulk_commit_group();
+                    stored = true;
                 }
             }
             const float lse_row = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
@@ -605,6 +650,8 @@ __global__ void __launch_bounds__(tc_threads<NT>(), NT == 2 ? 1 : 2)
             else if (valid && p.LSE)
                 p.LSE[(size_t(b) * p.Hq + head) * p.Lq + row] = lse_row;
         }
+        // the Q buffer stays allocated until the stores have read it
+        if (stored) bulk_wait_read_all();
         tc::fence_before_sync();
     }
 
@@ -648,7 +695,7 @@ int launch_tc_t(const PrefillLaunch& L, cudaStream_t stream) {
     if (items > 0x7fffffffLL) return ATTN_ERR_SHAPE;
     dim3 grid(unsigned(items), L.p.B, unsigned(L.p.splits > 1 ? L.p.splits : 1));
     prefill_tc_kernel<D, CAUSAL, ALIBI, MODE, NT>
-        <<<grid, tc_threads<NT>(), smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
+        <<<grid, tc_threads<NT>(), smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.tmO, L.p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
