@@ -432,14 +432,21 @@ __global__ void __launch_bounds__(tc_threads<NT>(), NT == 2 ? 1 : 2)
                 // serial counter); the row part b0 moves into the reference
                 // max: y = s * scale + slope * c here, and the exponent below
                 // is y - (m - b0), the same value as x - m with x = y + b0
+                // The column offsets slope * c come from four packed chains
+                // that step 8 columns per add (one add per key pair instead
+                // of two multiplies; 15 adds of rounding, < 2e-4 in log2 units)
                 const uint64_t sc2 = f2_pack(sl2, sl2);
+                const uint64_t step2 = f2_pack(8.f * slope_l2, 8.f * slope_l2);
+                uint64_t o2[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    o2[q] = f2_pack(slope_l2 * float(2 * q), slope_l2 * float(2 * q + 1));
 #pragma unroll
                 for (int c = 0; c < 128; c += 2) {
-                    const float o0 = slope_l2 * float(c);
-                    const float o1 = slope_l2 * float(c + 1);
-                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sc2, f2_pack(o0, o1)), s[c],
-                              s[c + 1]);
-                    mx4[(c >> 1) & 3] = max3(mx4[(c >> 1) & 3], s[c], s[c + 1]);
+                    const int q = (c >> 1) & 3;
+                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sc2, o2[q]), s[c], s[c + 1]);
+                    o2[q] = f2_add(o2[q], step2);
+                    mx4[q] = max3(mx4[q], s[c], s[c + 1]);
                 }
                 rel = slope_l2 * float(k0 - i_al);
             } else if (cap && !need_mask && !ALIBI) {
