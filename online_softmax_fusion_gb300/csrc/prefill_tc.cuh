@@ -433,6 +433,27 @@ __global__ void __launch_bounds__(tc_threads<NT>(), NT == 2 ? 1 : 2)
                     mx4[2] = max3(mx4[2], s[c + 4], s[c + 5]);
                     mx4[3] = max3(mx4[3], s[c + 6], s[c + 7]);
                 }
+            } else if (ALIBI && CAUSAL && need_mask && !cap && !EXTRA) {
+                // a causal ALiBi tile that crosses the diagonal or the key
+                // length: the unmasked form below plus one interval test per
+                // key (this row sees keys k0 .. k0 + chi of the tile)
+                const int chi = min(p.Lk - 1, i_al) - k0;
+                const uint64_t sc2 = f2_pack(sl2, sl2);
+                const uint64_t step2 = f2_pack(8.f * slope_l2, 8.f * slope_l2);
+                uint64_t o2[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    o2[q] = f2_pack(slope_l2 * float(2 * q), slope_l2 * float(2 * q + 1));
+#pragma unroll
+                for (int c = 0; c < 128; c += 2) {
+                    const int q = (c >> 1) & 3;
+                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sc2, o2[q]), s[c], s[c + 1]);
+                    o2[q] = f2_add(o2[q], step2);
+                    if (c > chi) s[c] = -INFINITY;
+                    if (c + 1 > chi) s[c + 1] = -INFINITY;
+                    mx4[q] = max3(mx4[q], s[c], s[c + 1]);
+                }
+                rel = slope_l2 * float(k0 - i_al);
             } else if (ALIBI && CAUSAL && !need_mask && !cap) {
                 // every key of this tile is at or before every row of the
                 // warp: bias = slope * (key - i') = slope * c + b0 with
