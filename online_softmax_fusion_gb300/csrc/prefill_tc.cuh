@@ -418,20 +418,39 @@ __global__ void __launch_bounds__(tc_threads<NT>(), NT == 2 ? 1 : 2)
                 if (p.window_right >= 0 && k0 + 127 > w_al + p.window_right) need_mask = true;
             }
             constexpr bool cap = CAPPED;
-            // x = s * scale (log2 domain) + bias, masked; on unmasked tiles
-            // without bias the scale is folded into the exp's FMA below
-            const bool fast = !need_mask && !ALIBI && !cap && sl2 > 0.f;
+            // x = s * scale (log2 domain) + bias, masked; without bias or
+            // cap the scale is folded into the exp's FMA below (masked keys
+            // hold -inf, which the positive scale keeps)
+            const bool fast = !ALIBI && !cap && sl2 > 0.f;
             // the part of every score of this tile that is left out of s[]
             // and carried in the reference max instead (ALiBi row offset)
             float rel = 0.f;
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            if (fast) {
+            if (fast && !need_mask) {
 #pragma unroll
                 for (int c = 0; c < 128; c += 8) {
                     mx4[0] = max3(mx4[0], s[c], s[c + 1]);
                     mx4[1] = max3(mx4[1], s[c + 2], s[c + 3]);
                     mx4[2] = max3(mx4[2], s[c + 4], s[c + 5]);
                     mx4[3] = max3(mx4[3], s[c + 6], s[c + 7]);
+                }
+            } else if (fast) {
+                // masked tile without bias or cap: this row's visible keys
+                // are one interval [klo, khi] (key length, causal, window);
+                // the raw scores outside it become -inf
+                int khi = p.Lk - 1;
+                if (CAUSAL) khi = min(khi, i_al);
+                int klo = 0;
+                if (EXTRA) {
+                    if (p.window_left >= 0) klo = max(klo, i_al - p.window_left);
+                    if (p.window_right >= 0) khi = min(khi, i_al + p.window_right);
+                }
+                const int clo = klo - k0, chi = khi - k0;
+#pragma unroll
+                for (int c = 0; c < 128; c += 2) {
+                    if (c < clo || c > chi) s[c] = -INFINITY;
+                    if (c + 1 < clo || c + 1 > chi) s[c + 1] = -INFINITY;
+                    mx4[(c >> 1) & 3] = max3(mx4[(c >> 1) & 3], s[c], s[c + 1]);
                 }
             } else if (ALIBI && CAUSAL && need_mask && !cap && !EXTRA) {
                 // a causal ALiBi tile that crosses the diagonal or the key
