@@ -425,6 +425,9 @@ __global__ void __launch_bounds__(tc_threads<NT>(), NT == 2 ? 1 : 2)
             // the part of every score of this tile that is left out of s[]
             // and carried in the reference max instead (ALiBi row offset)
             float rel = 0.f;
+            // causal ALiBi tile whose maximum provably cannot move the
+            // reference: the bias is applied in the exponential pass instead
+            bool lazy = false;
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (fast && !need_mask) {
 #pragma unroll
@@ -474,28 +477,50 @@ __global__ void __launch_bounds__(tc_threads<NT>(), NT == 2 ? 1 : 2)
                 }
                 rel = slope_l2 * float(k0 - i_al);
             } else if (ALIBI && CAUSAL && !need_mask && !cap) {
-                // every key of this tile is at or before every row of the
-                // warp: bias = slope * (key - i') = slope * c + b0 with
-                // b0 = slope * (k0 - i'). The column part is one FMA with the
-                // column index as an immediate (the loop is unrolled: no
-                // serial counter); the row part b0 moves into the reference
-                // max: y = s * scale + slope * c here, and the exponent below
-                // is y - (m - b0), the same value as x - m with x = y + b0
-                // The column offsets slope * c come from four packed chains
-                // that step 8 columns per add (one add per key pair instead
-                // of two multiplies; 15 adds of rounding, < 2e-4 in log2 units)
-                const uint64_t sc2 = f2_pack(sl2, sl2);
-                const uint64_t step2 = f2_pack(8.f * slope_l2, 8.f * slope_l2);
-                uint64_t o2[4];
+                // Bound first: every score of the tile is at most max(s) *
+                // scale + slope * 127 + slope * (k0 - i'). Scanned diagonal-
+                // first, the tiles after the first sit far enough below the
+                // reference that this bound already rules out a repair; then
+                // the exact maximum is not needed (the kept reference stays
+                // exact for O and l alike). Two-tile form only: in the one-tile
+                // form (168 registers) it spilled and measured slower.
+                if constexpr (NT == 2) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    o2[q] = f2_pack(slope_l2 * float(2 * q), slope_l2 * float(2 * q + 1));
+                    for (int c = 0; c < 128; c += 8) {
+                        mx4[0] = max3(mx4[0], s[c], s[c + 1]);
+                        mx4[1] = max3(mx4[1], s[c + 2], s[c + 3]);
+                        mx4[2] = max3(mx4[2], s[c + 4], s[c + 5]);
+                        mx4[3] = max3(mx4[3], s[c + 6], s[c + 7]);
+                    }
+                    const float smax = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+                    const float bound = smax * sl2 + slope_l2 * float(k0 + 127 - i_al);
+                    lazy = __all_sync(0xffffffffu, sl2 > 0.f && m != -INFINITY &&
+                                                       bound <= m + kRescaleThreshold);
 #pragma unroll
-                for (int c = 0; c < 128; c += 2) {
-                    const int q = (c >> 1) & 3;
-                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sc2, o2[q]), s[c], s[c + 1]);
-                    o2[q] = f2_add(o2[q], step2);
-                    mx4[q] = max3(mx4[q], s[c], s[c + 1]);
+                    for (int q = 0; q < 4; ++q) mx4[q] = -INFINITY;
+                }
+                if (!lazy) {
+                    // every key of this tile is at or before every row of the
+                    // warp: bias = slope * (key - i') = slope * c + b0 with
+                    // b0 = slope * (k0 - i'). The row part b0 moves into the
+                    // reference max: y = s * scale + slope * c here, and the
+                    // exponent below is y - (m - b0), the same value as x - m
+                    // with x = y + b0. The column offsets slope * c come from
+                    // four packed chains that step 8 columns per add (one add
+                    // per key pair; 15 adds of rounding, < 2e-4 in log2 units).
+                    const uint64_t sc2 = f2_pack(sl2, sl2);
+                    const uint64_t step2 = f2_pack(8.f * slope_l2, 8.f * slope_l2);
+                    uint64_t o2[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        o2[q] = f2_pack(slope_l2 * float(2 * q), slope_l2 * float(2 * q + 1));
+#pragma unroll
+                    for (int c = 0; c < 128; c += 2) {
+                        const int q = (c >> 1) & 3;
+                        f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sc2, o2[q]), s[c], s[c + 1]);
+                        o2[q] = f2_add(o2[q], step2);
+                        mx4[q] = max3(mx4[q], s[c], s[c + 1]);
+                    }
                 }
                 rel = slope_l2 * float(k0 - i_al);
             } else if (cap && !need_mask && !ALIBI) {
@@ -610,23 +635,57 @@ __global__ void __launch_bounds__(tc_threads<NT>(), NT == 2 ? 1 : 2)
             // the one-tile form runs at 168 registers: P goes out in quarters
             // so fewer packed values are live beside S
             constexpr int kPW = NT == 2 ? 32 : 16;   // packed columns per store
+            if (ALIBI && NT == 2 && lazy) {
+                // x - m = s * scale + slope * c + slope * (k0 - i') - m, the
+                // column and row parts from four packed chains started at
+                // slope * (k0 - i') - m
+                const uint64_t sc2 = f2_pack(sl2, sl2);
+                const uint64_t step2 = f2_pack(8.f * slope_l2, 8.f * slope_l2);
+                const float b0 = slope_l2 * float(k0 - i_al) - m_use;
+                uint64_t a2[4];
 #pragma unroll
-            for (int h = 0; h < 64 / kPW; ++h) {
-                uint32_t pk[kPW];
+                for (int q = 0; q < 4; ++q)
+                    a2[q] = f2_pack(fmaf(slope_l2, float(2 * q), b0),
+                                    fmaf(slope_l2, float(2 * q + 1), b0));
 #pragma unroll
-                for (int c2 = 0; c2 < kPW; ++c2) {
-                    const int c = h * 2 * kPW + 2 * c2;
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), mul2, neg2), x0, x1);
-                    const float p0 = ex2(x0);
-                    const float p1 = ex2(x1);
-                    sum2[c2 & 1] = f2_add(sum2[c2 & 1], f2_pack(p0, p1));
-                    pk[c2] = pack_bf16(p0, p1);
+                for (int h = 0; h < 64 / kPW; ++h) {
+                    uint32_t pk[kPW];
+#pragma unroll
+                    for (int c2 = 0; c2 < kPW; ++c2) {
+                        const int c = h * 2 * kPW + 2 * c2;
+                        const int q = (c >> 1) & 3;
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sc2, a2[q]), x0, x1);
+                        a2[q] = f2_add(a2[q], step2);
+                        const float p0 = ex2(x0);
+                        const float p1 = ex2(x1);
+                        sum2[c2 & 1] = f2_add(sum2[c2 & 1], f2_pack(p0, p1));
+                        pk[c2] = pack_bf16(p0, p1);
+                    }
+                    if constexpr (NT == 2)
+                        tc::tmem_st_32x32b_x32(tP + h * kPW, pk);
+                    else
+                        tc::tmem_st_32x32b_x16(tP + h * kPW, pk);
                 }
-                if constexpr (NT == 2)
-                    tc::tmem_st_32x32b_x32(tP + h * kPW, pk);
-                else
-                    tc::tmem_st_32x32b_x16(tP + h * kPW, pk);
+            } else {
+#pragma unroll
+                for (int h = 0; h < 64 / kPW; ++h) {
+                    uint32_t pk[kPW];
+#pragma unroll
+                    for (int c2 = 0; c2 < kPW; ++c2) {
+                        const int c = h * 2 * kPW + 2 * c2;
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), mul2, neg2), x0, x1);
+                        const float p0 = ex2(x0);
+                        const float p1 = ex2(x1);
+                        sum2[c2 & 1] = f2_add(sum2[c2 & 1], f2_pack(p0, p1));
+                        pk[c2] = pack_bf16(p0, p1);
+                    }
+                    if constexpr (NT == 2)
+                        tc::tmem_st_32x32b_x32(tP + h * kPW, pk);
+                    else
+                        tc::tmem_st_32x32b_x16(tP + h * kPW, pk);
+                }
             }
             float sa, sb, sc, sd;
             f2_unpack(sum2[0], sa, sb);
