@@ -893,7 +893,8 @@ def run_ours(args):
         LSE = torch.empty((pc.B, pc.Hq, pc.Lq), dtype=torch.float32, device=dev)
 
         def prefill():
-            attn.prefill(q, k, v, causal=True, scale=pc.scale, out=O, lse=LSE)
+            attn.prefill(q, k, v, causal=True, scale=pc.scale, out=O, lse=LSE,
+                         softcap=args.softcap)
         launches.append(("prefill", prefill))
     if do_d:
         din = W.make_decode_inputs(dc, dev)
@@ -1073,7 +1074,8 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": bench_config(args.kernel, pc, dc, world),
+            "config": dict(bench_config(args.kernel, pc, dc, world),
+                           **({"softcap": args.softcap} if args.softcap else {})),
             "roofline": roof,
             "decode": decode_obj,
             "e2e": e2e,
@@ -1098,6 +1100,9 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--softcap", type=float, default=0.0,
+                    help="--kernel prefill only: the prefill with this SoftCap (profiling "
+                         "captures of the capped variant; 0 = none)")
     ap.add_argument("--rms-form", choices=["auto", "fused", "two_pass"], default=None,
                     help="--kernel rmsnorm: call the workspace entry with this form "
                          "(default: the single fused kernel)")
@@ -1115,6 +1120,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.softcap and (args.kernel != "prefill" or args.impl != "ours"):
+        ap.error("--softcap applies to --kernel prefill only")
     if args.impl == "reference":
         return run_reference(args)
     if args.kernel == "rmsnorm":
