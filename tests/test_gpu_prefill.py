@@ -75,6 +75,31 @@ def test_prefill_small_cases(attn, impl, B, Hq, Hkv, Lq, Lk, d, causal, alibi):
 
 
 @pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("Hq,Lq", [(8, 1024), (4, 1000)])
+def test_alibi_far_keys_dominate(attn, impl, Hq, Lq):
+    """Causal ALiBi where the keys far from the diagonal carry much larger
+    scores (K rows scaled x8 below the first 256 keys): scanned diagonal-
+    first, later tiles raise the row maximum, so the bound that lets a warp
+    skip the exact maximum fails and the reference is repaired mid-row, on
+    top of the masked diagonal tile and a ragged tail."""
+    d = 128
+    q = _rand((1, Hq, Lq, d), 71)
+    k = _rand((1, 2, Lq, d), 72)
+    v = _rand((1, 2, Lq, d), 73)
+    kf = k.float()
+    kf[:, :, : Lq - 256] *= 8.0
+    k = kf.to(torch.bfloat16)
+    slopes = W.alibi_slopes(Hq)
+    scale = 1.0 / d ** 0.5
+    O, L = attn.prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=scale,
+                        alibi_slopes=slopes.cuda(), impl=impl)
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    Or, Lr = attention_ref(q, k, v, scale=scale, causal=True, alibi_slopes=slopes)
+    assert_attention_close(O, L, Or, Lr)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
 def test_large_logits_stay_finite(attn, impl):
     """q and K scaled x8 (logits in the hundreds): the repaired online softmax
     stays finite and matches the oracle."""
