@@ -28,12 +28,18 @@
 //
 // Per KV step j, for each tile t (the two tiles alternate on the tensor core):
 //   TMA warp : K_j, V_j -> 5-slot shared-memory ring (128-byte swizzle)
-//   MMA warp : O_t += P_t V_j (A from TMEM), then S_t = Q_t K_{j+1}^T
+//   MMA warp : O_t += P_t V_j (A from TMEM), then S_t = Q_t K_j'^T for the
+//              tile j' scanned next
 //   softmax t: S_t (TMEM) -> registers, row max, p = 2^(x - m), row sum,
 //              P_t (bf16) -> TMEM, O_t rescale in TMEM if needed
-// The commit that signals S_t^{j+1} also covers the PV product issued before
-// it, so when the softmax sees S_t^{j+1}, O_t is final for step j. One thread
+// The commit that signals S_t for j' also covers the PV product issued
+// before it, so when the softmax sees it, O_t is final for step j. One thread
 // owns one query row (TMEM lane = row): row reductions need no shuffles.
+// KV tiles are scanned in ascending order, or diagonal-first under causal
+// ALiBi (the bias then peaks on the first tile) and causal windows. SoftCap
+// evaluates tanh as a polynomial on the FMA pipe where |score / cap| allows
+// it. O leaves through each tile's Q buffer as bulk tensor stores in the
+// paired-head and capped forms, as direct row stores elsewhere.
 #pragma once
 
 #include "common.cuh"
