@@ -169,6 +169,26 @@ def test_rmsnorm_matmul_validation_before_launch(L):
     assert L.attn_rmsnorm_matmul_splits(1, 64, 8) == 1   # one K step
 
 
+def test_rmsnorm_matmul_ws_validation_before_launch(L):
+    """The workspace entry (two-pass form): form, workspace and its size are
+    checked before anything reaches the device."""
+    assert L.attn_rmsnorm_matmul_ws_bytes(0, 64) == 0
+    assert L.attn_rmsnorm_matmul_ws_bytes(4, 256) == 2048 + 2 * 256   # X*G, then E and s
+    need = L.attn_rmsnorm_matmul_ws_bytes(4, 256)
+
+    def ws(form, work=P, nbytes=need, X=P, B=4, H=256, D=128):
+        return L.attn_rmsnorm_matmul_ws(X, P, P, P, None, B, H, D, 0.0, form, work, nbytes, None)
+    assert ws(3) == 8 and ws(-1) == 8            # unknown form
+    assert ws(2, work=None) == 1                 # the two-pass form needs the workspace
+    assert ws(2, nbytes=need - 16) == 4          # too small
+    assert ws(2, work=MIS) == 7                  # misaligned
+    assert ws(2, X=None) == 1
+    assert ws(2, H=100) == 3                     # H not a multiple of 8
+    assert ws(0, B=0) == 2 and ws(0, D=-8) == 2  # the automatic form checks shapes first
+    assert ws(1, X=None) == 1                    # the fused form ignores the workspace
+    assert ws(1, work=None, H=100) == 3
+
+
 def test_prefill_splitkv_validation_before_launch(L):
     def sk(S, ws=P, wsb=1 << 30, Q=P):
         return L.attn_prefill_splitkv(Q, P, P, P, None, 1, 4, 2, 128, 128, 128, 1, 0.1, None, S,
