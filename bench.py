@@ -532,9 +532,8 @@ def measure_other_workloads(attn, W, dev, peaks, checks):
         ms_chained = graph_time(lambda: fn_rms(True), 4, replays=5) / len(wcopies)
         # the workspace entry (two-pass form for batch tiles of 128 rows and more)
         ms_ws = graph_time(fn_ws, 4, replays=5) / len(wcopies)
-        two_pass = attn.lib().attn_rmsnorm_matmul_ws_bytes(cfg.B, cfg.H) > 0 and cfg.B >= 128
         ms = min(ms_chained, ms_ws)
-        form = "chained" if ms_chained <= ms_ws else ("two_pass" if two_pass else "fused")
+        form = "chained" if ms_chained <= ms_ws else "two_pass"
         byts = rmsnorm_matmul_bytes(cfg.B, cfg.H, cfg.D)
         fl = rmsnorm_matmul_flops(cfg.B, cfg.H, cfg.D)
         gbs = byts / (ms * 1e-3) / 1e9

@@ -312,8 +312,8 @@ int attn_rmsnorm_matmul_chained(const void* X, const void* G, const void* W, voi
  *                           fused form (X ⊙ G rounded to bf16 once); RMS may
  *                           differ from the fused form's in the last bits
  *                           (another summation order)
- *   ATTN_RMS_FORM_AUTO      two-pass when the batch tile is 128 rows or more
- *                           (the fused converters limit large tiles), else fused
+ *   ATTN_RMS_FORM_AUTO      the two-pass form (measured faster than the fused
+ *                           kernel at batches 16 to 256 at H = D = 4096)
  *   workspace        device, >= attn_rmsnorm_matmul_ws_bytes(B, H) bytes,
  *                    16-byte aligned, caller-owned; contents are scratch
  * Other arguments, results and errors as attn_rmsnorm_matmul (automatic

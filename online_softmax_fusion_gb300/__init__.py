@@ -317,8 +317,9 @@ def rmsnorm_matmul(x, g, w, eps=0.0, splits=0, out=None, rms=None, with_rms=Fals
     sqrt(mean(x^2) + eps). x [B,H], g [H], w [H,D] bf16 CUDA. Returns
     (O bf16 [B,D], RMS fp32 [B] or None). batch_tile / splits: 0 = auto.
     form: None = the single fused kernel; "auto" / "fused" / "two_pass" go
-    through the workspace entry (a separate conversion pass for large batch
-    tiles); workspace: uint8 CUDA tensor, allocated when not given."""
+    through the workspace entry ("auto": the two-pass form, a separate
+    conversion pass then the product); workspace: uint8 CUDA tensor,
+    allocated when not given."""
     _req(x, "x", torch.bfloat16, 2)
     _req(g, "g", torch.bfloat16, 1)
     _req(w, "w", torch.bfloat16, 2)

@@ -514,10 +514,9 @@ int attn_rmsnorm_matmul_ws(const void* X, const void* G, const void* W, void* O,
     if (form < ATTN_RMS_FORM_AUTO || form > ATTN_RMS_FORM_TWO_PASS) return ATTN_ERR_VALUE;
     if (form == ATTN_RMS_FORM_AUTO) {
         if (B <= 0 || H <= 0 || D <= 0) return ATTN_ERR_SHAPE;
-        // the fused converters keep up with the tensor core for batch tiles
-        // below 128 rows; from there the separate conversion pass is faster
-        form = rms_geometry(B, H, D, 0, 0).NB >= 128 ? ATTN_RMS_FORM_TWO_PASS
-                                                    : ATTN_RMS_FORM_FUSED;
+        // measured faster than the fused kernel at every batch tried
+        // (16 ... 256 rows at H = D = 4096)
+        form = ATTN_RMS_FORM_TWO_PASS;
     }
     if (form == ATTN_RMS_FORM_FUSED)
         return rmsnorm_matmul_impl(X, G, W, O, rms, B, H, D, eps, 0, 0, 0, stream);

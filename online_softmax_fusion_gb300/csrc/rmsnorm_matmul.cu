@@ -551,35 +551,44 @@ __global__ void __launch_bounds__(rm_threads<CVT>(), CVT == 8 ? 2 : 1)
 // The conversion pass of the two-kernel form: X ⊙ G rounded to bf16 (the
 // product's operand, the same rounding as the fused converter) and, per row,
 // the reference exponent E (2^E above the row's largest |x|) and the sum s of
-// (x 2^-E)^2 (exact power-of-two scaling: no square can overflow). One warp
-// per row; the row is read twice (the second time from L1/L2).
-__global__ void __launch_bounds__(256) rms_prep_kernel(const __nv_bfloat16* __restrict__ X,
-                                                       const __nv_bfloat16* __restrict__ G,
-                                                       __nv_bfloat16* __restrict__ Xg,
-                                                       int* __restrict__ e_out,
-                                                       float* __restrict__ s_out, int B, int H) {
+// (x 2^-E)^2 (exact power-of-two scaling: no square can overflow). One CTA
+// of 256 threads per row (one warp per row on B / 8 CTAs measured ~10 us at
+// batch 256, most of it before the product could start); the row is read
+// twice, the second time from L1.
+constexpr int kPrepThreads = 256;
+
+__global__ void __launch_bounds__(kPrepThreads) rms_prep_kernel(
+    const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ G,
+    __nv_bfloat16* __restrict__ Xg, int* __restrict__ e_out, float* __restrict__ s_out, int B,
+    int H) {
     // the product kernel, launched as this kernel's dependent, may start
     // streaming W now; it waits for this grid before reading Xg or (E, s)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int row = int(blockIdx.x) * 8 + int(threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= B) return;
+    __shared__ uint32_t red_u[kPrepThreads / 32];
+    __shared__ float red_f[kPrepThreads / 32];
+    const int row = int(blockIdx.x);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const uint4* x = reinterpret_cast<const uint4*>(X + size_t(row) * H);
     const uint4* g = reinterpret_cast<const uint4*>(G);
     uint4* xg = reinterpret_cast<uint4*>(Xg + size_t(row) * H);
     const int nc = H / 8;
     uint32_t mm = 0u;
-    for (int c = lane; c < nc; c += 32) {
+    for (int c = threadIdx.x; c < nc; c += kPrepThreads) {
         const uint4 v = x[c];
         mm = bf16x2_maxabs(mm, bf16x2_maxabs(bf16x2_maxabs(v.x, v.y), bf16x2_maxabs(v.z, v.w)));
     }
     mm &= 0x7fff7fffu;
     uint32_t mb = max(mm & 0xffffu, mm >> 16);
     for (int o = 16; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    if (lane == 0) red_u[wid] = mb;
+    __syncthreads();
+    mb = red_u[0];
+#pragma unroll
+    for (int w = 1; w < kPrepThreads / 32; ++w) mb = max(mb, red_u[w]);
     const int E = mb != 0u ? max(int(mb >> 7) - 126, kMinExp) : kEmptyExp;
     const float sc = mb != 0u ? ldexpf(1.f, -E) : 0.f;
     float acc = 0.f;
-    for (int c = lane; c < nc; c += 32) {
+    for (int c = threadIdx.x; c < nc; c += kPrepThreads) {
         uint4 v = x[c];
         acc = sq2(v.x, sc, acc);
         acc = sq2(v.y, sc, acc);
@@ -593,15 +602,20 @@ __global__ void __launch_bounds__(256) rms_prep_kernel(const __nv_bfloat16* __re
         xg[c] = v;
     }
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
+    if (lane == 0) red_f[wid] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = red_f[0];
+#pragma unroll
+        for (int w = 1; w < kPrepThreads / 32; ++w) t += red_f[w];
         e_out[row] = E;
-        s_out[row] = acc;
+        s_out[row] = t;
     }
 }
 
 int launch_rmsnorm_prep(const __nv_bfloat16* X, const __nv_bfloat16* G, __nv_bfloat16* Xg,
                         int* e_out, float* s_out, int B, int H, cudaStream_t stream) {
-    rms_prep_kernel<<<unsigned((B + 7) / 8), 256, 0, stream>>>(X, G, Xg, e_out, s_out, B, H);
+    rms_prep_kernel<<<unsigned(B), kPrepThreads, 0, stream>>>(X, G, Xg, e_out, s_out, B, H);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -235,7 +235,8 @@ def test_two_pass_parity(B, H, D, eps):
     ref = rmsnorm_matmul_ref(x.cpu(), g.cpu(), w.cpu(), eps)
     _check(O, ref)
     np.testing.assert_allclose(rms.cpu().numpy(), rms_ref(x.cpu(), eps), rtol=2e-5)
-    np.testing.assert_allclose(rms.cpu().numpy(), rms1.cpu().numpy(), rtol=2e-6)
+    # both are fp32 sums of the same exactly scaled squares, in other orders
+    np.testing.assert_allclose(rms.cpu().numpy(), rms1.cpu().numpy(), rtol=1e-5)
     diff = torch.abs(O.float() - O1.float())
     assert torch.all(diff <= 2.0 ** -7 * torch.abs(O1.float()) + 1e-30)
 
