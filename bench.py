@@ -523,17 +523,20 @@ def measure_other_workloads(attn, W, dev, peaks, checks):
             for wc in wcopies:
                 attn.rmsnorm_matmul(rin["x"], rin["g"], wc, out=Orm, chained=chained)
 
-        def fn_ws():
+        def fn_ws(chained=False):
             for wc in wcopies:
-                attn.rmsnorm_matmul(rin["x"], rin["g"], wc, out=Orm, form="auto", workspace=wsb)
+                attn.rmsnorm_matmul(rin["x"], rin["g"], wc, out=Orm, form="auto", workspace=wsb,
+                                    chained=chained)
         ms_plain = graph_time(lambda: fn_rms(False), 4, replays=5) / len(wcopies)
         # a stack of calls with constant weights: each launch overlaps the
         # end of the one before (programmatic dependent launch)
         ms_chained = graph_time(lambda: fn_rms(True), 4, replays=5) / len(wcopies)
-        # the workspace entry (two-pass form for batch tiles of 128 rows and more)
+        # the workspace entry (two-pass form), plainly and chained
         ms_ws = graph_time(fn_ws, 4, replays=5) / len(wcopies)
-        ms = min(ms_chained, ms_ws)
-        form = "chained" if ms_chained <= ms_ws else "two_pass"
+        ms_ws_chained = graph_time(lambda: fn_ws(True), 4, replays=5) / len(wcopies)
+        forms = {"chained": ms_chained, "two_pass": ms_ws, "two_pass_chained": ms_ws_chained}
+        form = min(forms, key=forms.get)
+        ms = forms[form]
         byts = rmsnorm_matmul_bytes(cfg.B, cfg.H, cfg.D)
         fl = rmsnorm_matmul_flops(cfg.B, cfg.H, cfg.D)
         gbs = byts / (ms * 1e-3) / 1e9
@@ -543,10 +546,12 @@ def measure_other_workloads(attn, W, dev, peaks, checks):
                     "frac_bf16": tf / peaks["bf16_tflops"], "bytes": byts, "flops": fl,
                     "splits": attn.lib().attn_rmsnorm_matmul_splits(cfg.B, cfg.H, cfg.D),
                     "ms_single_launch": ms_plain, "ms_chained": ms_chained,
-                    "ms_workspace_entry": ms_ws, "form": form,
+                    "ms_workspace_entry": ms_ws, "ms_workspace_entry_chained": ms_ws_chained,
+                    "form": form,
                     "timing": "cuda graph replay of 5 back-to-back calls, W rotated over 5 "
-                              "copies (> L2); ms = the faster of the chained calls and the "
-                              "workspace entry (form names it); ms_single_launch: plain calls"})
+                              "copies (> L2); ms = the fastest of the chained fused calls and "
+                              "the workspace entry, plain or chained (form names it); "
+                              "ms_single_launch: plain fused calls"})
         checks.append({"workload": name, "kind": "rmsnorm", "x": rin["x"][:3].cpu(),
                        "g": rin["g"].cpu(), "w": rin["w"].cpu(), "O": Orm[:3].cpu()})
         del rin, wcopies, Orm

@@ -326,6 +326,21 @@ int attn_rmsnorm_matmul_ws(const void* X, const void* G, const void* W, void* O,
                            int B, int H, int D, float eps, int form, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/*
+ * attn_rmsnorm_matmul_ws_chained - attn_rmsnorm_matmul_ws for calls that
+ * follow one another on a stream with constant weights (no counterpart in
+ * the pages: a launch option of this library, as attn_rmsnorm_matmul_chained).
+ * The first kernel of the call (the conversion pass, or the fused kernel) is
+ * launched as a programmatic dependent of the kernel before it on the stream
+ * and waits for that kernel before it reads X or the workspace; in the
+ * two-pass form the product kernel follows the pass as before. Caller's
+ * promise: W is not written by the kernel that precedes the call. Arguments,
+ * results and errors as attn_rmsnorm_matmul_ws.
+ */
+int attn_rmsnorm_matmul_ws_chained(const void* X, const void* G, const void* W, void* O,
+                                   float* rms, int B, int H, int D, float eps, int form,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* The split count attn_rmsnorm_matmul chooses when given 0 (negative status on
  * invalid sizes). */
 int attn_rmsnorm_matmul_splits(int B, int H, int D);

@@ -70,6 +70,8 @@ SIGNATURES = {
     "attn_rmsnorm_matmul_ws": (_c_int, [_c_void_p] * 5 + [_c_int] * 3 + [_c_float, _c_int,
                                                                        _c_void_p, ctypes.c_size_t,
                                                                        _c_void_p]),
+    "attn_rmsnorm_matmul_ws_chained": (_c_int, [_c_void_p] * 5 + [_c_int] * 3 +
+                                       [_c_float, _c_int, _c_void_p, ctypes.c_size_t, _c_void_p]),
     "attn_decode_num_splits": (_c_int, [_c_int] * 5),
     "attn_decode_split_len": (_c_int, [_c_int] * 2),
     "attn_decode_workspace_bytes": (ctypes.c_size_t, [_c_int] * 4),
@@ -332,16 +334,17 @@ def rmsnorm_matmul(x, g, w, eps=0.0, splits=0, out=None, rms=None, with_rms=Fals
     if rms is None and with_rms:
         rms = torch.empty((B,), dtype=torch.float32, device=x.device)
     if form is not None:
-        if chained or splits or batch_tile:
+        if splits or batch_tile:
             raise ValueError("the workspace entry chooses its own tiling")
         if form not in RMS_FORMS:
             raise ValueError(f"form must be one of {sorted(RMS_FORMS)}")
         nbytes = rmsnorm_matmul_ws_bytes(B, H)
         if workspace is None:
             workspace = torch.empty((max(nbytes, 1),), dtype=torch.uint8, device=x.device)
-        st = lib().attn_rmsnorm_matmul_ws(_ptr(x), _ptr(g), _ptr(w), _ptr(out), _ptr(rms), B, H,
-                                          D, float(eps), RMS_FORMS[form], _ptr(workspace),
-                                          workspace.numel() * workspace.element_size(), _stream())
+        fn = lib().attn_rmsnorm_matmul_ws_chained if chained else lib().attn_rmsnorm_matmul_ws
+        st = fn(_ptr(x), _ptr(g), _ptr(w), _ptr(out), _ptr(rms), B, H, D, float(eps),
+                RMS_FORMS[form], _ptr(workspace), workspace.numel() * workspace.element_size(),
+                _stream())
     elif chained:
         # launched as a programmatic dependent of the kernel before it on the
         # stream; w must not be written by that kernel (automatic tiling)

@@ -508,9 +508,37 @@ size_t attn_rmsnorm_matmul_ws_bytes(int B, int H) {
     return rms_ws_xg_bytes(B, H) + 2 * rms_ws_vec_bytes(B);
 }
 
+}  // extern "C"
+
+namespace {
+int rmsnorm_ws_impl(const void* X, const void* G, const void* W, void* O, float* rms, int B,
+                    int H, int D, float eps, int form, void* workspace, size_t workspace_bytes,
+                    int chained, void* stream);
+}  // namespace
+
+extern "C" {
+
 int attn_rmsnorm_matmul_ws(const void* X, const void* G, const void* W, void* O, float* rms,
                            int B, int H, int D, float eps, int form, void* workspace,
                            size_t workspace_bytes, void* stream) {
+    return rmsnorm_ws_impl(X, G, W, O, rms, B, H, D, eps, form, workspace, workspace_bytes, 0,
+                           stream);
+}
+
+int attn_rmsnorm_matmul_ws_chained(const void* X, const void* G, const void* W, void* O,
+                                   float* rms, int B, int H, int D, float eps, int form,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+    return rmsnorm_ws_impl(X, G, W, O, rms, B, H, D, eps, form, workspace, workspace_bytes, 1,
+                           stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int rmsnorm_ws_impl(const void* X, const void* G, const void* W, void* O, float* rms, int B,
+                    int H, int D, float eps, int form, void* workspace, size_t workspace_bytes,
+                    int chained, void* stream) {
     if (form < ATTN_RMS_FORM_AUTO || form > ATTN_RMS_FORM_TWO_PASS) return ATTN_ERR_VALUE;
     if (form == ATTN_RMS_FORM_AUTO) {
         if (B <= 0 || H <= 0 || D <= 0) return ATTN_ERR_SHAPE;
@@ -519,14 +547,14 @@ int attn_rmsnorm_matmul_ws(const void* X, const void* G, const void* W, void* O,
         form = ATTN_RMS_FORM_TWO_PASS;
     }
     if (form == ATTN_RMS_FORM_FUSED)
-        return rmsnorm_matmul_impl(X, G, W, O, rms, B, H, D, eps, 0, 0, 0, stream);
+        return rmsnorm_matmul_impl(X, G, W, O, rms, B, H, D, eps, 0, 0, chained, stream);
     if (!workspace) return ATTN_ERR_NULL;
     if (B > 0 && H > 0 && workspace_bytes < attn_rmsnorm_matmul_ws_bytes(B, H))
         return ATTN_ERR_WORKSPACE;
-    return rmsnorm_matmul_impl(X, G, W, O, rms, B, H, D, eps, 0, 0, 0, stream, workspace);
+    return rmsnorm_matmul_impl(X, G, W, O, rms, B, H, D, eps, 0, 0, chained, stream, workspace);
 }
 
-}  // extern "C"
+}  // namespace
 
 namespace {
 
@@ -584,7 +612,8 @@ int rmsnorm_matmul_impl(const void* X, const void* G, const void* W, void* O, fl
         if ((st = make_map(&L.tmX, xg, H, B, 1, g.NB))) return st;
         if ((st = make_map(&L.tmW, W, D, H, 1, 64))) return st;
         if ((st = launch_rmsnorm_prep(static_cast<const __nv_bfloat16*>(X),
-                                      static_cast<const __nv_bfloat16*>(G), xg, e, sq, B, H, cs)))
+                                      static_cast<const __nv_bfloat16*>(G), xg, e, sq, B, H,
+                                      chained, cs)))
             return st;
         L.p.pre = 1;
         L.p.stats_e = e;

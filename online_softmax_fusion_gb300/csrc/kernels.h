@@ -137,8 +137,10 @@ struct RmsLaunch {
 constexpr int kRmsMaxWStages = 12;
 constexpr int kRmsMaxXStages = 8;
 int launch_rmsnorm_matmul(const RmsLaunch& L, cudaStream_t stream);
-// The conversion pass: Xg = X ⊙ G (bf16) and per row (E, s), one warp per row.
+// The conversion pass: Xg = X ⊙ G (bf16) and per row (E, s), one CTA per row;
+// chained: launched as a programmatic dependent of the kernel before it.
 int launch_rmsnorm_prep(const __nv_bfloat16* X, const __nv_bfloat16* G, __nv_bfloat16* Xg,
-                        int* e_out, float* s_out, int B, int H, cudaStream_t stream);
+                        int* e_out, float* s_out, int B, int H, int chained,
+                        cudaStream_t stream);
 
 }  // namespace attn

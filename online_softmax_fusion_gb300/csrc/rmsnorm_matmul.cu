@@ -560,10 +560,13 @@ constexpr int kPrepThreads = 256;
 __global__ void __launch_bounds__(kPrepThreads) rms_prep_kernel(
     const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ G,
     __nv_bfloat16* __restrict__ Xg, int* __restrict__ e_out, float* __restrict__ s_out, int B,
-    int H) {
+    int H, int chained) {
     // the product kernel, launched as this kernel's dependent, may start
     // streaming W now; it waits for this grid before reading Xg or (E, s)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // chained: X may be written, and the workspace still read, by the kernel
+    // before this one on the stream; it has finished once this returns
+    if (chained) asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ uint32_t red_u[kPrepThreads / 32];
     __shared__ float red_f[kPrepThreads / 32];
     const int row = int(blockIdx.x);
@@ -614,9 +617,23 @@ __global__ void __launch_bounds__(kPrepThreads) rms_prep_kernel(
 }
 
 int launch_rmsnorm_prep(const __nv_bfloat16* X, const __nv_bfloat16* G, __nv_bfloat16* Xg,
-                        int* e_out, float* s_out, int B, int H, cudaStream_t stream) {
-    rms_prep_kernel<<<unsigned(B), kPrepThreads, 0, stream>>>(X, G, Xg, e_out, s_out, B, H);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+                        int* e_out, float* s_out, int B, int H, int chained,
+                        cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(B));
+    cfg.blockDim = dim3(kPrepThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = chained ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, rms_prep_kernel, X, G, Xg, e_out, s_out, B, H, chained) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
 }
 
 namespace {

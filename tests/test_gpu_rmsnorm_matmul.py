@@ -299,3 +299,31 @@ def test_two_pass_rejects_small_workspace_and_unknown_form():
     O, _ = attn.rmsnorm_matmul(x, g, w, form="fused", workspace=small)
     torch.cuda.synchronize()
     _check(O, rmsnorm_matmul_ref(x.cpu(), g.cpu(), w.cpu()))
+
+
+@pytest.mark.parametrize("B,H,D", [(16, 4096, 4096), (5, 328, 328), (256, 1024, 1024)])
+def test_two_pass_chained_stack_of_layers(B, H, D):
+    """Chained two-pass calls sharing one workspace: each call's X is the
+    previous call's output, and its conversion pass rewrites the workspace
+    the previous product kernel read. Every layer equals, bit for bit, the
+    same call made plainly, and matches the oracle."""
+    x, g, _ = _inputs(B, H, D, 9)
+    ws = [_inputs(B, H, D, 40 + i)[2] for i in range(4)]
+    work = torch.empty((attn.rmsnorm_matmul_ws_bytes(B, H),), dtype=torch.uint8, device=DEV)
+    outs, rms = [], []
+    cur = x
+    for w in ws:
+        O, R = attn.rmsnorm_matmul(cur, g, w, with_rms=True, form="two_pass", chained=True,
+                                   workspace=work)
+        outs.append(O)
+        rms.append(R)
+        cur = O
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    cur = x
+    for w, O, R in zip(ws, outs, rms):
+        _check(O, rmsnorm_matmul_ref(cur, g, w))
+        O_plain, R_plain = attn.rmsnorm_matmul(cur, g, w, with_rms=True, form="two_pass")
+        torch.cuda.synchronize()
+        assert torch.equal(O, O_plain) and torch.equal(R, R_plain)
+        cur = O
